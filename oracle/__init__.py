@@ -1,0 +1,176 @@
+"""CPU oracle for the Benchmark Streaming operations -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg
+(``bench.py``: ``cpu_baseline`` and ``--impl reference``) may import this
+package.  The library (``order_fem_cg_gb300``) never does, and the oracle
+never imports the library: the two share only the seeded inputs of
+``bsinputs``.
+
+Every operation is a plain loop in ``oracle.c`` (binary64, explicit fma,
+-ffp-contract=off), wrapped here with numpy for argument marshalling.  The
+sources each function follows are cited in ``oracle.c``:
+
+  * "Portable high-order finite element kernels I: Streaming Operations"
+    (the BS1-BS7 definitions, eq. (3), the gather/scatter kernel text);
+  * "GPU accelerated spectral finite elements on all-hex meshes"
+    (local-to-global and global-to-local tables);
+  * Ogita, Rump, Oishi (2005), Dot2, for the accurate reductions.
+
+Pins (checked by ``tests/test_oracle_pins.py`` against facts fixed by the
+pages and by mathematics, not against this code): every function below is
+pinned; none is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64 = ctypes.c_int64
+_dbl = ctypes.c_double
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (no fast-math, no contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+             "-shared", "-o", tmp, _SRC, "-lm"],
+            check=True,
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_copy.argtypes = [_i64, _f64p, _f64p]
+        lib.oracle_axpy.argtypes = [_i64, _dbl, _f64p, _dbl, _f64p]
+        lib.oracle_dot_plain.argtypes = [_i64, _f64p, _f64p]
+        lib.oracle_dot_plain.restype = _dbl
+        lib.oracle_dot2.argtypes = [_i64, _f64p, _f64p]
+        lib.oracle_dot2.restype = _dbl
+        lib.oracle_cg_update.argtypes = [_i64, _dbl, _f64p, _f64p, _f64p, _f64p]
+        lib.oracle_scatter.argtypes = [_i64, _i32p, _f64p, _f64p]
+        lib.oracle_gather.argtypes = [_i64, _i64, _i32p, _f64p, _f64p]
+        lib.oracle_box_scatter_ids.argtypes = [ctypes.c_int, ctypes.c_int, _i32p, _i32p,
+                                               ctypes.c_int, _i32p]
+        for f in (lib.oracle_copy, lib.oracle_axpy, lib.oracle_cg_update, lib.oracle_scatter,
+                  lib.oracle_gather, lib.oracle_box_scatter_ids):
+            f.restype = None
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def copy(x):
+    """BS1: y = x."""
+    x = _f64(x)
+    y = np.empty_like(x)
+    _load().oracle_copy(x.size, x, y)
+    return y
+
+
+def axpy(alpha, x, beta, y):
+    """BS2: returns fma(alpha, x_i, beta*y_i) (y is not modified)."""
+    x = _f64(x)
+    out = np.array(y, dtype=np.float64, copy=True, order="C")
+    assert out.size == x.size
+    _load().oracle_axpy(x.size, float(alpha), x, float(beta), out)
+    return out
+
+
+def dot(x, y):
+    """BS4: Dot2 accurate inner product, summed in index order."""
+    x, y = _f64(x), _f64(y)
+    assert x.size == y.size
+    return float(_load().oracle_dot2(x.size, x, y))
+
+
+def dot_plain(x, y):
+    """Plain sequential inner product (every step rounded)."""
+    x, y = _f64(x), _f64(y)
+    assert x.size == y.size
+    return float(_load().oracle_dot_plain(x.size, x, y))
+
+
+def norm(x):
+    """BS3: x.x (the squared 2-norm), by Dot2."""
+    x = _f64(x)
+    return float(_load().oracle_dot2(x.size, x, x))
+
+
+def cg_update(alpha, p, Ap, x, r):
+    """BS5: returns (x + alpha p, r - alpha Ap, r_new . r_new); inputs untouched."""
+    p, Ap = _f64(p), _f64(Ap)
+    xo = np.array(x, dtype=np.float64, copy=True, order="C")
+    ro = np.array(r, dtype=np.float64, copy=True, order="C")
+    n = p.size
+    assert Ap.size == n and xo.size == n and ro.size == n
+    lib = _load()
+    lib.oracle_cg_update(n, float(alpha), p, Ap, xo, ro)
+    return xo, ro, float(lib.oracle_dot2(n, ro, ro))
+
+
+def scatter(ids, qG):
+    """BS7: q_L = Z q_G through the local-to-global table (negative id -> 0)."""
+    ids, qG = _i32(ids), _f64(qG)
+    qL = np.empty(ids.size, dtype=np.float64)
+    _load().oracle_scatter(ids.size, ids, qG, qL)
+    return qL
+
+
+def gather(ids, qL, NG):
+    """BS6: q_G = Z^T q_L, each global value summed in ascending local index."""
+    ids, qL = _i32(ids), _f64(qL)
+    assert ids.size == qL.size
+    qG = np.empty(int(NG), dtype=np.float64)
+    _load().oracle_gather(ids.size, int(NG), ids, qL, qG)
+    return qG
+
+
+def box_scatter_ids(E, N, elem_perm, node_perm, mask_boundary=False):
+    """Local-to-global table of an E^3 box mesh of degree N (int32, -1 = masked)."""
+    ep, npm = _i32(elem_perm), _i32(node_perm)
+    assert ep.size == E ** 3 and npm.size == (E * N + 1) ** 3
+    ids = np.empty(E ** 3 * (N + 1) ** 3, dtype=np.int32)
+    _load().oracle_box_scatter_ids(int(E), int(N), ep, npm, int(bool(mask_boundary)), ids)
+    return ids
+
+
+def cg_sequence(ids, pG, xG, rG, rr):
+    """One CG iteration's streaming sequence with the identity local operator.
+
+    p_L = Z p_G; Ap_G = Z^T p_L; pAp = p_G . Ap_G; alpha = rr / pAp;
+    x += alpha p, r -= alpha Ap with rr_new = r.r; finally rnorm = r.r.
+    Returns a dict of every intermediate.
+    """
+    pG = _f64(pG)
+    pL = scatter(ids, pG)
+    ApG = gather(ids, pL, pG.size)
+    pAp = dot(pG, ApG)
+    alpha = float(rr) / pAp
+    x1, r1, rr_new = cg_update(alpha, pG, ApG, xG, rG)
+    rnorm = norm(r1)
+    return dict(pL=pL, ApG=ApG, pAp=pAp, alpha=alpha, x=x1, r=r1, rr_new=rr_new, rnorm=rnorm)

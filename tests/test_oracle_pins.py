@@ -1,0 +1,424 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU needed).
+
+Each check below ties an oracle function to something the pages or the
+mathematics fix independently of the oracle's code:
+
+  * the published SplitMix64 test vector (input generator);
+  * the node counts N_L = K(p+1)^3, N_G = (EN+1)^3 of the workload meshes;
+  * geometric brute force: physical GLL node coordinates, deduplicated, give
+    the global nodes (two locals share a global id iff they share a point);
+  * the closed-form multiplicity histogram C(3,k) a^k b^(3-k);
+  * gather(scatter(u)) = m * u, sum(q_G) = sum(q_L), dense Z / Z^T products;
+  * closed-form norms and dots, exact rational arithmetic (Fraction) for the
+    fused multiply-adds, and the Ogita-Rump-Oishi error bound for Dot2.
+
+The last group plants mistakes in copies of oracle steps and checks that the
+pins catch them.
+"""
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import bsinputs as gen
+import oracle
+
+U = 2.0 ** -53  # unit roundoff of binary64
+
+
+# ----------------------------------------------------------------------------
+# Independent geometry: physical coordinates of every local node.
+# ----------------------------------------------------------------------------
+
+def gll_nodes(N):
+    """Gauss-Lobatto-Legendre nodes on [-1, 1]: the end points and the roots of P_N'."""
+    if N == 1:
+        return np.array([-1.0, 1.0])
+    inner = np.sort(np.polynomial.legendre.Legendre.basis(N).deriv().roots().real)
+    return np.concatenate([[-1.0], inner, [1.0]])
+
+
+def local_coords(E, N, elem_perm):
+    """(x, y, z) of each local node: element lattice cell mapped to [0,1]^3,
+    reference GLL node (r_i, s_j, t_k) mapped affinely into it."""
+    r = gll_nodes(N)
+    q = N + 1
+    K = E ** 3
+    e = np.asarray(elem_perm, dtype=np.int64)
+    ex, ey, ez = e % E, (e // E) % E, e // (E * E)
+    # local node n = i + q (j + q k) inside a slot, i fastest
+    n = np.arange(q ** 3)
+    i, j, k = n % q, (n // q) % q, n // (q * q)
+    x = (ex[:, None] + (1.0 + r[i])[None, :] / 2.0) / E
+    y = (ey[:, None] + (1.0 + r[j])[None, :] / 2.0) / E
+    z = (ez[:, None] + (1.0 + r[k])[None, :] / 2.0) / E
+    return np.stack([x.reshape(-1), y.reshape(-1), z.reshape(-1)], axis=1).reshape(K * q ** 3, 3)
+
+
+def geometric_ids(E, N, elem_perm, node_perm, mask=False):
+    """Expected local-to-global table from geometry alone: the lattice number
+    of a node is its rank along each axis among the distinct coordinates."""
+    c = local_coords(E, N, elem_perm)
+    M = E * N + 1
+    g = []
+    for a in range(3):
+        ua = np.unique(c[:, a])
+        assert ua.size == M
+        g.append(np.searchsorted(ua, c[:, a]))
+    L = g[0] + M * (g[1] + M * g[2])
+    ids = np.asarray(node_perm)[L].astype(np.int32)
+    if mask:
+        on_b = np.any((c == 0.0) | (c == 1.0), axis=1)
+        ids[on_b] = -1
+    return ids
+
+
+def ids_match_geometry(E, N, elem_perm, node_perm, ids, mask=False):
+    c = local_coords(E, N, elem_perm)
+    _, inv = np.unique(c, axis=0, return_inverse=True)
+    inv = inv.reshape(-1)
+    # two local nodes share a global id iff they share a point
+    pairs = set(zip(inv.tolist(), np.asarray(ids).tolist()))
+    if not mask:
+        if len(pairs) != (E * N + 1) ** 3 or len(set(i for i, _ in pairs)) != len(pairs):
+            return False
+        if len(set(g for _, g in pairs)) != len(pairs):
+            return False
+    return np.array_equal(np.asarray(ids), geometric_ids(E, N, elem_perm, node_perm, mask))
+
+
+def multiplicity_closed_form(E, N):
+    a, b = E - 1, E * (N - 1) + 2
+    return {2 ** k: math.comb(3, k) * a ** k * b ** (3 - k) for k in range(4)}
+
+
+def mesh(cfg_or_EN, seed=12345, flags=gen.SHUFFLE_ELEMS | gen.PERMUTE_GLOBAL):
+    if isinstance(cfg_or_EN, gen.MeshConfig):
+        cfg = cfg_or_EN
+    else:
+        E, N = cfg_or_EN
+        cfg = gen.MeshConfig("t", E, N, seed, flags)
+    ep, npm = gen.mesh_perms(cfg)
+    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+    return cfg, ep, npm, ids
+
+
+# ----------------------------------------------------------------------------
+# Input generator pins
+# ----------------------------------------------------------------------------
+
+def test_splitmix64_published_vector(golden):
+    expect = [int(r[0]) for r in golden("splitmix64_seed1234567.txt")]
+    # tag 0 makes the stream key equal to the seed
+    assert [int(v) for v in gen.draws(1234567, 0, 5)] == expect
+    assert [gen.mix64_int(1234567 + (i + 1) * gen.GAMMA) for i in range(5)] == expect
+    # counter-based: a window equals the corresponding slice
+    assert np.array_equal(gen.draws(1234567, 0, 3, start=2), gen.draws(1234567, 0, 5)[2:])
+
+
+def test_uniform_values_exact_form():
+    z = gen.draws(7, 3, 2000) >> np.uint64(11)
+    u = gen.uniform_pm1(7, 3, 2000)
+    for k, v in zip(z.tolist(), u.tolist()):
+        assert Fraction(v) == Fraction(2 * k + 1, 2 ** 53) - 1
+    assert np.all(np.abs(u) < 1.0) and np.all(u != 0.0)
+    assert abs(u.mean()) < 0.05
+
+
+def test_permutation_definition():
+    n = 3000
+    keys = gen.draws(99, 1, n).tolist()
+    expect = sorted(range(n), key=lambda i: (keys[i], i))
+    p = gen.permutation(99, 1, n)
+    assert p.tolist() == expect
+    assert np.array_equal(np.sort(p), np.arange(n))
+
+
+def test_normal_moments():
+    v = gen.normal(5, 3, 200000)
+    assert abs(v.mean()) < 0.01 and abs(v.std() - 1.0) < 0.01
+
+
+# ----------------------------------------------------------------------------
+# Mesh numbering pins
+# ----------------------------------------------------------------------------
+
+def test_mesh_sizes(golden):
+    for name, E, N, NL, NG in golden("mesh_sizes.txt"):
+        cfg = gen.CONFIGS[name]
+        assert (cfg.E, cfg.N) == (int(E), int(N))
+        assert cfg.NL == int(NL) and cfg.NG == int(NG)
+        assert cfg.NL == cfg.K * (cfg.N + 1) ** 3
+
+
+@pytest.mark.parametrize("E,N,flags", [
+    (2, 2, 0), (2, 2, 3), (3, 3, 3), (2, 5, 3), (1, 1, 0), (1, 4, 3), (4, 2, 1), (3, 1, 2)])
+def test_numbering_matches_geometry(E, N, flags):
+    cfg, ep, npm, ids = mesh((E, N), seed=1000 + E * 10 + N, flags=flags)
+    assert ids.size == cfg.NL
+    assert ids.min() >= 0 and ids.max() < cfg.NG
+    assert ids_match_geometry(E, N, ep, npm, ids)
+
+
+@pytest.mark.parametrize("E,N", [(2, 2), (3, 3), (1, 2)])
+def test_masked_numbering_matches_geometry(E, N):
+    flags = gen.SHUFFLE_ELEMS | gen.PERMUTE_GLOBAL | gen.MASK_BOUNDARY
+    cfg, ep, npm, ids = mesh((E, N), seed=77, flags=flags)
+    assert ids_match_geometry(E, N, ep, npm, ids, mask=True)
+    M = E * N + 1
+    # masked globals = the box-boundary lattice nodes
+    unmasked_globals = np.unique(ids[ids >= 0])
+    assert unmasked_globals.size == max(M - 2, 0) ** 3
+
+
+def test_multiplicity_closed_form_golden(golden):
+    for E, N, c1, c2, c4, c8 in golden("multiplicity.txt"):
+        E, N = int(E), int(N)
+        assert multiplicity_closed_form(E, N) == {1: int(c1), 2: int(c2), 4: int(c4), 8: int(c8)}
+
+
+@pytest.mark.parametrize("which", ["tiny", "mid", (2, 2), (5, 4), (1, 3)])
+def test_gather_of_ones_is_multiplicity(which):
+    cfg, ep, npm, ids = mesh(gen.CONFIGS[which] if isinstance(which, str) else which)
+    m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
+    vals, counts = np.unique(m, return_counts=True)
+    hist = dict(zip(vals.astype(int).tolist(), counts.tolist()))
+    expect = {k: v for k, v in multiplicity_closed_form(cfg.E, cfg.N).items() if v}
+    assert hist == expect
+    assert int(m.sum()) == cfg.NL
+
+
+def test_dense_Z_brute_force_2x2x2():
+    """Dense 216 x 125 Boolean Z from coordinates; oracle scatter = Z q_G and
+    gather = Z^T q_L, on integer data where every order is exact."""
+    E, N = 2, 2
+    cfg, ep, npm, ids = mesh((E, N), seed=4242)
+    gids = geometric_ids(E, N, ep, npm)
+    Z = np.zeros((cfg.NL, cfg.NG))
+    Z[np.arange(cfg.NL), gids] = 1.0
+    assert np.all(Z.sum(axis=1) == 1.0)                 # one nonzero per row of Z
+    qG = gen.integers_dyadic(1, 3, cfg.NG)
+    qL = gen.integers_dyadic(1, 4, cfg.NL)
+    assert np.array_equal(oracle.scatter(ids, qG), Z @ qG)
+    assert np.array_equal(oracle.gather(ids, qL, cfg.NG), Z.T @ qL)
+
+
+@pytest.mark.parametrize("which", ["tiny", (3, 3)])
+def test_gather_scatter_identities(which):
+    cfg, ep, npm, ids = mesh(gen.CONFIGS[which] if isinstance(which, str) else which)
+    m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
+    u = gen.integers_dyadic(cfg.seed, gen.TAG_U, cfg.NG)
+    assert np.array_equal(oracle.gather(ids, oracle.scatter(ids, u), cfg.NG), m * u)
+    qL = gen.uniform_pm1(cfg.seed, gen.TAG_P, cfg.NL)
+    qG = oracle.gather(ids, qL, cfg.NG)
+    assert abs(math.fsum(qG) - math.fsum(qL)) <= 1e-12 * math.fsum(np.abs(qL))
+
+
+def test_masked_scatter_and_gather():
+    flags = gen.SHUFFLE_ELEMS | gen.PERMUTE_GLOBAL | gen.MASK_BOUNDARY
+    cfg, ep, npm, ids = mesh((3, 2), seed=5, flags=flags)
+    qG = gen.uniform_pm1(1, 2, cfg.NG)
+    qL = oracle.scatter(ids, qG)
+    assert np.all(qL[ids < 0] == 0.0) and np.all(np.signbit(qL[ids < 0]) == False)
+    assert np.array_equal(qL[ids >= 0], qG[ids[ids >= 0]])
+    m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
+    c = local_coords(3, 2, ep)
+    interior = ~np.any((c == 0.0) | (c == 1.0), axis=1)
+    g_int = np.unique(ids[interior])
+    assert np.all(m[g_int] >= 1)
+    rest = np.setdiff1d(np.arange(cfg.NG), g_int)
+    assert np.all(m[rest] == 0.0)
+
+
+def _gather_by_rows(ids, qL, NG):
+    """Brute force: for each global node, its local copies sorted ascending, summed from +0.0."""
+    out = []
+    for g in range(NG):
+        ls = np.sort(np.nonzero(ids == g)[0])
+        s = 0.0
+        for l in ls:
+            s = s + float(qL[l])
+        out.append(s)
+    return np.array(out)
+
+
+def order_probe(ids, NG, first_big):
+    """Values whose row sum depends on order: per row, one 1.0 and 2^-53 elsewhere."""
+    qL = np.full(ids.size, 2.0 ** -53)
+    for g in range(NG):
+        ls = np.sort(np.nonzero(ids == g)[0])
+        qL[ls[0] if first_big else ls[-1]] = 1.0
+    return qL
+
+
+def test_gather_sum_order_is_ascending_local_index():
+    cfg, ep, npm, ids = mesh((2, 2), seed=31)
+    for first_big in (True, False):
+        qL = order_probe(ids, cfg.NG, first_big)
+        got = oracle.gather(ids, qL, cfg.NG)
+        assert np.array_equal(got, _gather_by_rows(ids, qL, cfg.NG))
+    qL = gen.uniform_pm1(3, 3, cfg.NL)
+    assert np.array_equal(oracle.gather(ids, qL, cfg.NG), _gather_by_rows(ids, qL, cfg.NG))
+    # +0.0 start: a single -0.0 contribution gives +0.0
+    qL = np.full(cfg.NL, -0.0)
+    assert not np.any(np.signbit(oracle.gather(ids, qL, cfg.NG)))
+
+
+# ----------------------------------------------------------------------------
+# Vector operation pins
+# ----------------------------------------------------------------------------
+
+def test_copy_is_bitwise_identity():
+    x = np.array([0.0, -0.0, 1.5, np.inf, -np.inf, 5e-324, -2.2250738585072014e-308, 1e308])
+    bits = np.concatenate([x.view(np.uint64), np.array([0x7FF8000000000123, 0xFFF0000000000001],
+                                                        dtype=np.uint64)])
+    x = bits.view(np.float64)
+    assert np.array_equal(oracle.copy(x).view(np.uint64), bits)
+    assert oracle.copy(np.zeros(0)).size == 0
+
+
+def _round(fr):
+    return float(fr)   # CPython int/int true division rounds correctly (ties to even)
+
+
+@pytest.mark.parametrize("beta", [1.0, -0.5, 0.3])
+def test_axpy_matches_exact_rational(beta):
+    n = 3000
+    x = gen.uniform_pm1(11, 1, n) * 1e3
+    y = gen.uniform_pm1(11, 2, n)
+    alpha = 0.37
+    got = oracle.axpy(alpha, x, beta, y)
+    for i in range(n):
+        by = _round(Fraction(beta) * Fraction(y[i]))    # beta * y_i rounded first
+        assert got[i] == _round(Fraction(alpha) * Fraction(x[i]) + Fraction(by))
+
+
+def test_cg_update_matches_exact_rational():
+    n = 2000
+    p, Ap, x, r = (gen.uniform_pm1(21, t, n) for t in (4, 5, 7, 6))
+    alpha = 0.6180339887
+    x1, r1, rr = oracle.cg_update(alpha, p, Ap, x, r)
+    for i in range(n):
+        assert x1[i] == _round(Fraction(alpha) * Fraction(p[i]) + Fraction(x[i]))
+        assert r1[i] == _round(-Fraction(alpha) * Fraction(Ap[i]) + Fraction(r[i]))
+    exact = sum(Fraction(v) * Fraction(v) for v in r1.tolist())
+    assert abs(Fraction(rr) - exact) <= 2 * U * exact
+
+
+def test_norm_closed_forms():
+    n = 1000003
+    assert oracle.norm(np.full(n, 0.5)) == n / 4
+    n = 100003
+    i = np.arange(n, dtype=np.float64)
+    exact = (n - 1) * n * (2 * n - 1) // 6
+    assert abs(Fraction(oracle.norm(i)) - exact) <= U * exact
+    assert oracle.dot(i, np.ones(n)) == n * (n - 1) // 2
+    assert oracle.norm(np.zeros(0)) == 0.0 and not math.copysign(1.0, oracle.norm(np.zeros(0))) < 0
+
+
+def ill_conditioned_pair(n, seed):
+    """x, y whose exact dot is tiny next to sum |x_i y_i|: the last term cancels the rest."""
+    x = gen.uniform_pm1(seed, 1, n)
+    y = gen.uniform_pm1(seed, 2, n)
+    s = math.fsum(x[:-1] * y[:-1])
+    x[-1] = 1.0
+    y[-1] = -s
+    return x, y
+
+
+def _exact_dot(x, y):
+    return sum(Fraction(a) * Fraction(b) for a, b in zip(x.tolist(), y.tolist()))
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_dot2_error_bound(seed):
+    """Ogita-Rump-Oishi: |Dot2 - s| <= u|s| + gamma_n^2 sum|x_i y_i|; the plain
+    sum only meets gamma_n sum|x_i y_i|."""
+    n = 4000
+    x, y = ill_conditioned_pair(n, seed)
+    s = _exact_dot(x, y)
+    absum = sum(abs(Fraction(a) * Fraction(b)) for a, b in zip(x.tolist(), y.tolist()))
+    g = n * U / (1 - n * U)
+    d2 = Fraction(oracle.dot(x, y))
+    assert abs(d2 - s) <= U * abs(s) + Fraction(g * g) * absum
+    dp = Fraction(oracle.dot_plain(x, y))
+    assert abs(dp - s) <= Fraction(g) * absum
+
+
+# ----------------------------------------------------------------------------
+# Planted mistakes: copies of oracle steps with one plausible error each must
+# fail the pins above.
+# ----------------------------------------------------------------------------
+
+def _ids_ij_swapped(E, N, ep, npm):
+    ids = oracle.box_scatter_ids(E, N, ep, npm)
+    q = N + 1
+    return ids.reshape(-1, q, q, q).transpose(0, 1, 3, 2).reshape(-1).copy()
+
+
+def _ids_wrong_element_axis(E, N, ep, npm):
+    # element number read as ez + E(ey + E ex)
+    e = np.asarray(ep)
+    ep2 = (e // (E * E)) + E * (((e // E) % E) + E * (e % E))
+    return oracle.box_scatter_ids(E, N, ep2.astype(np.int32), npm)
+
+
+def test_planted_numbering_mistakes_are_caught():
+    E, N = 3, 2
+    cfg, ep, npm, ids = mesh((E, N), seed=8)
+    assert ids_match_geometry(E, N, ep, npm, ids)
+    assert not ids_match_geometry(E, N, ep, npm, _ids_ij_swapped(E, N, ep, npm))
+    assert not ids_match_geometry(E, N, ep, npm, _ids_wrong_element_axis(E, N, ep, npm))
+    # node permutation applied in the inverse direction
+    inv = np.empty_like(npm)
+    inv[npm] = np.arange(npm.size, dtype=np.int32)
+    bad = oracle.box_scatter_ids(E, N, ep, inv)
+    assert not ids_match_geometry(E, N, ep, npm, bad)
+
+
+def test_planted_gather_mistakes_are_caught():
+    cfg, ep, npm, ids = mesh((2, 2), seed=31)
+    qL = order_probe(ids, cfg.NG, first_big=True)
+    expect = _gather_by_rows(ids, qL, cfg.NG)
+    # descending local order
+    desc = np.zeros(cfg.NG)
+    for l in range(cfg.NL - 1, -1, -1):
+        desc[ids[l]] += qL[l]
+    assert not np.array_equal(desc, expect)
+    # dropped last local entry, seen on generic data
+    qL = gen.uniform_pm1(3, 3, cfg.NL)
+    drop = oracle.gather(ids[:-1], qL[:-1], cfg.NG)
+    assert not np.array_equal(drop, _gather_by_rows(ids, qL, cfg.NG))
+
+
+def test_planted_reduction_mistakes_are_caught():
+    n = 4000
+    x, y = ill_conditioned_pair(n, 1)
+    s = _exact_dot(x, y)
+    absum = sum(abs(Fraction(a) * Fraction(b)) for a, b in zip(x.tolist(), y.tolist()))
+    g = n * U / (1 - n * U)
+    bound = U * abs(s) + Fraction(g * g) * absum
+    # Dot2 without the TwoProduct error term: only the TwoSum half
+    p = q = 0.0
+    for a, b in zip(x.tolist(), y.tolist()):
+        h = a * b
+        t = p + h
+        z = t - p
+        q += (p - (t - z)) + (h - z)
+        p = t
+    assert abs(Fraction(p + q) - s) > bound
+    # the plain sum
+    assert abs(Fraction(oracle.dot_plain(x, y)) - s) > bound
+
+
+def test_planted_axpy_mistake_is_caught():
+    n = 3000
+    x = gen.uniform_pm1(11, 1, n) * 1e3
+    y = gen.uniform_pm1(11, 2, n)
+    alpha = 0.37
+    exact = [_round(Fraction(alpha) * Fraction(a) + Fraction(b)) for a, b in zip(x, y)]
+    unfused = alpha * x + y          # two roundings instead of one fma
+    assert not np.array_equal(unfused, np.array(exact))
+    assert np.array_equal(oracle.axpy(alpha, x, 1.0, y), np.array(exact))
