@@ -1,0 +1,615 @@
+#!/usr/bin/env python3
+"""Bench of the seven Benchmark Streaming operations (BS1-BS7) on GB300.
+
+Default run (one JSON line on stdout, rank 0):
+  one step = the whole hot path on the stress mesh (64^3 hexahedra, degree
+  5: N_L = 56,623,104 local and N_G = 33,076,161 global nodes, element
+  order shuffled, global ids permuted): BS1 copy, BS2 AXPY, BS3 norm, BS4
+  dot, BS5 fused CG update at length N_L, BS6 gather, BS7 scatter, and one
+  CG iteration's streaming sequence (scatter, gather, dot, fused update,
+  norm) on global-length vectors.  Every operation works on its own
+  buffers, all larger than L2, so no operation reads what the previous one
+  left in L2.
+  value = algorithmic bytes of the step / device time of the step (GB/s),
+  timed with CUDA events on the launching stream over exactly --steps
+  steps after --warmup steps.  Per-kernel times come from events between
+  the launches; the dominant kernel's figures form the `roofline` object.
+
+Other modes:
+  --impl reference   the CPU oracle timed on a bounded sample of the same
+                     workload (the reference arm).
+  --sweep            BS1-BS5 at n = 2^10 .. 2^27, host-timed launch->sync
+                     as the pages time, with the T(B) = T0 + B/Wmax fit.
+  --probe            binary64 FMA pipe throughput probe.
+  --config NAME      another mesh workload (tiny, mid, large, stress).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bsinputs as gen  # noqa: E402
+
+METRIC = "achieved HBM GB/s per BS1–BS7 kernel and fraction of measured GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SRC = {
+    "copy": "bs_vec.cu", "axpy": "bs_vec.cu", "norm": "bs_vec.cu", "dot": "bs_vec.cu",
+    "cg_update": "bs_vec.cu", "gather": "bs_gs.cu", "scatter": "bs_gs.cu",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--config", choices=sorted(gen.CONFIGS), default="stress")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-sample", type=float, default=0.25,
+                    help="fraction of the step the oracle runs for cpu_baseline")
+    ap.add_argument("--ref-sample", type=float, default=1.0 / 32,
+                    help="fraction of the step per reference-arm step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--probe", action="store_true")
+    ap.add_argument("--soak", type=float, default=1.5,
+                    help="seconds of untimed steps before warm-up (clock sampling)")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def src_sha(name):
+    with open(os.path.join(ROOT, "order_fem_cg_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def ncu_traffic(kernel, config):
+    """ncu DRAM bytes per launch of `kernel`, if captured on the current source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)["kernels"][kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("src_sha256") != src_sha(KERNEL_SRC[kernel]) or rec.get("config") != config:
+        return None
+    return rec.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        rows = [r for r in self.rows if num(r[0]) is not None]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in rows if (num(r[3]) or 0) >= 50] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(num(r[0]) for r in loaded),
+                "sm_max_mhz": max(num(r[1]) or 0 for r in loaded),
+                "power_w_max": max(num(r[2]) or 0 for r in loaded),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# --------------------------------------------------------------- workload
+
+class Workload:
+    """Device buffers and the launch list of one step on a mesh configuration."""
+
+    N_VEC_L = ("a", "b", "c", "d", "e", "f", "g", "P", "AP", "X", "R", "qL1", "qL2", "pL")
+    N_VEC_G = ("qG1", "qG2", "pG", "ApG", "xG", "rG")
+
+    def __init__(self, cfg, torch, bs, device):
+        self.cfg, self.torch, self.bs, self.device = cfg, torch, bs, device
+        self.mesh = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+        if self.mesh.validate() != bs.BS_OK:
+            raise RuntimeError("mesh tables failed validation")
+        self.tables = self.mesh.to_device(device.index)
+        NL, NG = cfg.NL, cfg.NG
+        self.NL, self.NG = NL, NG
+        s = cfg.seed
+        # host inputs (seeded); several device buffers share values
+        self.h = {
+            "u": gen.uniform_pm1(s, gen.TAG_U, NL), "p": gen.uniform_pm1(s, gen.TAG_P, NL),
+            "Ap": gen.uniform_pm1(s, gen.TAG_AP, NL), "r": gen.uniform_pm1(s, gen.TAG_R, NL),
+            "x": gen.uniform_pm1(s, gen.TAG_X, NL),
+            "qG": gen.uniform_pm1(s, gen.TAG_U + 32, NG), "pG": gen.uniform_pm1(s, gen.TAG_P + 32, NG),
+            "xG": gen.uniform_pm1(s, gen.TAG_X + 32, NG), "rG": gen.uniform_pm1(s, gen.TAG_R + 32, NG),
+        }
+        self.src = {"a": "u", "c": "p", "d": "r", "e": "Ap", "f": "x", "g": "u", "P": "p",
+                    "AP": "Ap", "X": "x", "R": "r", "qL1": "u", "qG2": "qG", "pG": "pG",
+                    "xG": "xG", "rG": "rG"}
+        self.v = {}
+        for k in self.N_VEC_L:
+            self.v[k] = torch.empty(NL, dtype=torch.float64, device=device)
+        for k in self.N_VEC_G:
+            self.v[k] = torch.empty(NG, dtype=torch.float64, device=device)
+        for k, src in self.src.items():
+            self.v[k].copy_(torch.from_numpy(self.h[src]))
+        self.rr_host = float(np.dot(self.h["rG"], self.h["rG"]))
+        self.sc = {k: torch.zeros(1, dtype=torch.float64, device=device)
+                   for k in ("norm", "dot", "rdotr", "rr", "pAp", "rr_new", "rnorm")}
+        self.sc["rr"].fill_(self.rr_host)
+        torch.cuda.synchronize()
+        pm = bs_perf()
+        t = self.tables
+        self.bytes = {
+            "copy": pm.bytes_copy(NL), "axpy": pm.bytes_axpy(NL), "norm": pm.bytes_norm(NL),
+            "dot": pm.bytes_dot(NL), "cg_update": pm.bytes_cg_update(NL),
+            "gather": pm.bytes_gather(NL, NG, t.nnz, t.nblocks),
+            "scatter": pm.bytes_scatter(NL, NG),
+            "cg_iteration": pm.bytes_cg_iteration(NL, NG, t.nnz, t.nblocks),
+        }
+        self.launches = {"copy": 1, "axpy": 1, "norm": 1, "dot": 1, "cg_update": 1, "gather": 1,
+                         "scatter": 1, "cg_iteration": 5}
+        self.names = list(self.bytes)
+
+    @property
+    def step_bytes(self):
+        return sum(self.bytes.values())
+
+    @property
+    def launches_per_step(self):
+        return sum(self.launches.values())
+
+    def op(self, name, stream):
+        bs, v, sc, cfg = self.bs, self.v, self.sc, self.cfg
+        if name == "copy":
+            bs.bs_copy(v["a"], v["b"], stream)
+        elif name == "axpy":
+            bs.bs_axpy(cfg.alpha, v["c"], cfg.beta, v["d"], stream)
+        elif name == "norm":
+            bs.bs_norm(v["e"], sc["norm"], stream)
+        elif name == "dot":
+            bs.bs_dot(v["f"], v["g"], sc["dot"], stream)
+        elif name == "cg_update":
+            bs.bs_cg_update(v["P"], v["AP"], v["X"], v["R"], alpha=cfg.alpha, rdotr=sc["rdotr"],
+                            stream=stream)
+        elif name == "gather":
+            bs.bs_gather(self.tables, v["qL1"], v["qG1"], stream)
+        elif name == "scatter":
+            bs.bs_scatter(self.tables, v["qG2"], v["qL2"], stream)
+        elif name == "cg_iteration":
+            bs.bs_cg_iteration(self.tables, v["pG"], v["pL"], v["ApG"], v["xG"], v["rG"], sc["rr"],
+                               sc["pAp"], sc["rr_new"], sc["rnorm"], stream)
+        else:
+            raise KeyError(name)
+
+    def step(self, stream, events=None):
+        for i, name in enumerate(self.names):
+            self.op(name, stream)
+            if events is not None:
+                events[i + 1].record(stream)
+
+    # -- end to end: host buffers in, host buffers out
+    INPUTS = ("a", "c", "d", "e", "f", "g", "P", "AP", "X", "R", "qL1", "qG2", "pG", "xG", "rG")
+    OUTPUTS = ("b", "d", "X", "R", "qG1", "qL2", "xG", "rG")
+
+    def pin_host(self):
+        torch = self.torch
+        self.hin = {k: torch.from_numpy(self.h[self.src[k]]).pin_memory() for k in self.INPUTS}
+        self.hout = {k: torch.empty(self.v[k].numel(), dtype=torch.float64).pin_memory()
+                     for k in self.OUTPUTS}
+        self.hsc_in = torch.tensor([self.rr_host], dtype=torch.float64).pin_memory()
+        self.hsc_out = torch.empty(len(self.sc), dtype=torch.float64).pin_memory()
+        self.sc_cat = torch.empty(len(self.sc), dtype=torch.float64, device=self.device)
+
+    @property
+    def h2d_bytes(self):
+        return sum(t.numel() * 8 for t in self.hin.values()) + 8
+
+    @property
+    def d2h_bytes(self):
+        return sum(t.numel() * 8 for t in self.hout.values()) + 8 * len(self.sc)
+
+    def step_e2e(self, stream):
+        torch = self.torch
+        with torch.cuda.stream(stream):
+            for k, t in self.hin.items():
+                self.v[k].copy_(t, non_blocking=True)
+            self.sc["rr"].copy_(self.hsc_in, non_blocking=True)
+            self.step(stream)
+            for k, t in self.hout.items():
+                t.copy_(self.v[k], non_blocking=True)
+            torch.cat([self.sc[k] for k in self.sc], out=self.sc_cat)
+            self.hsc_out.copy_(self.sc_cat, non_blocking=True)
+
+
+def bs_perf():
+    from order_fem_cg_gb300 import perfmodel
+    return perfmodel
+
+
+# --------------------------------------------------------- oracle (CPU) leg
+
+class OracleSample:
+    """The oracle on a bounded sample of the step: every operation on the
+    first `frac` of its local-length range (the CG sequence on the first
+    `frac` of its global-length vectors and local entries)."""
+
+    def __init__(self, cfg, frac, host=None):
+        import oracle
+        self.oracle = oracle
+        self.cfg = cfg
+        ep, npm = gen.mesh_perms(cfg)
+        self.ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+        NL, NG = cfg.NL, cfg.NG
+        self.m = max(1, int(NL * frac))
+        self.mg = max(1, int(NG * frac))
+        self.frac = frac
+        s = cfg.seed
+        h = host or {}
+        self.u = h.get("u", gen.uniform_pm1(s, gen.TAG_U, NL))[: self.m]
+        self.p = h.get("p", gen.uniform_pm1(s, gen.TAG_P, NL))[: self.m]
+        self.Ap = h.get("Ap", gen.uniform_pm1(s, gen.TAG_AP, NL))[: self.m]
+        self.r = h.get("r", gen.uniform_pm1(s, gen.TAG_R, NL))[: self.m]
+        self.x = h.get("x", gen.uniform_pm1(s, gen.TAG_X, NL))[: self.m]
+        self.qG = h.get("qG", gen.uniform_pm1(s, gen.TAG_U + 32, NG))
+        self.pG = h.get("pG", gen.uniform_pm1(s, gen.TAG_P + 32, NG))
+        self.xG = h.get("xG", gen.uniform_pm1(s, gen.TAG_X + 32, NG))
+        self.rG = h.get("rG", gen.uniform_pm1(s, gen.TAG_R + 32, NG))
+        pm = bs_perf()
+        # the full step's algorithmic bytes (blockStarts omitted: negligible)
+        full = (pm.bytes_copy(NL) + pm.bytes_axpy(NL) + pm.bytes_norm(NL) + pm.bytes_dot(NL)
+                + pm.bytes_cg_update(NL) + pm.bytes_gather(NL, NG, NL, 0) + pm.bytes_scatter(NL, NG)
+                + pm.bytes_cg_iteration(NL, NG, NL, 0))
+        self.bytes = frac * full
+
+    def step(self):
+        o, cfg, m, mg = self.oracle, self.cfg, self.m, self.mg
+        o.copy(self.u)
+        o.axpy(cfg.alpha, self.p, cfg.beta, self.r)
+        o.norm(self.Ap)
+        o.dot(self.x, self.u)
+        o.cg_update(cfg.alpha, self.p, self.Ap, self.x, self.r)
+        o.gather(self.ids[:m], self.u, cfg.NG)
+        o.scatter(self.ids[:m], self.qG)
+        # CG sequence on the sample: scatter/gather over m local entries,
+        # vector operations over the first mg global entries
+        pL = o.scatter(self.ids[:m], self.pG)
+        ApG = o.gather(self.ids[:m], pL, cfg.NG)
+        pAp = o.dot(self.pG[:mg], ApG[:mg])
+        _, r1, _ = o.cg_update(1.0 / (pAp or 1.0), self.pG[:mg], ApG[:mg], self.xG[:mg],
+                               self.rG[:mg])
+        o.norm(r1)
+
+    def describe(self):
+        return (f"oracle (single-threaded C, Dot2 reductions) on {self.frac:.4g} of the step: "
+                f"BS1-BS5 on the first {self.m} of {self.cfg.NL} entries, gather/scatter over the "
+                f"first {self.m} local entries, the CG sequence on the first {self.mg} of "
+                f"{self.cfg.NG} global entries; GB/s = sampled algorithmic bytes / wall time")
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = gen.CONFIGS[args.config]
+    samp = OracleSample(cfg, args.ref_sample)
+    for _ in range(args.warmup):
+        samp.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        samp.step()
+    dt = time.perf_counter() - t0
+    value = samp.bytes * args.steps / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": samp.describe()},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg, gpus):
+    return {
+        "workload": f"{cfg.name} box mesh E={cfg.E} N={cfg.N}: {cfg.K} hexahedra, N_L={cfg.NL} local "
+                    f"and N_G={cfg.NG} global nodes, elements shuffled and global ids permuted by "
+                    f"seed {cfg.seed:#x}; fp64 U(-1,1) data, alpha={cfg.alpha}, beta={cfg.beta}; step = "
+                    "BS1-BS5 at n=N_L, BS6 gather, BS7 scatter, one CG iteration's sequence at n=N_G",
+        "l2": (f"inputs larger than L2: every operation streams its own buffers of >= "
+               f"{8 * cfg.NG / 1e6:.0f} MB (L2 is 129 MB)" if 8 * cfg.NG > 129e6 else
+               f"inputs NOT larger than L2 ({8 * cfg.NL / 1e6:.1f} MB per local vector, L2 129 MB): "
+               "figures include L2 reuse"),
+        "parallelism": f"replicas x{gpus} (independent meshes, no collective)",
+    }
+
+
+# ------------------------------------------------------------ GPU leg
+
+def init_dist(torch, world, local_rank):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend, device_id=torch.device("cuda", local_rank)
+                            if backend == "nccl" else None)
+    return dist
+
+
+def run_gpu(args):
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = init_dist(torch, world, local_rank)
+    import order_fem_cg_gb300 as bs
+
+    cfg = gen.CONFIGS[args.config]
+    wl = Workload(cfg, torch, bs, device)
+    stream = torch.cuda.Stream(device)
+    peak, peak_src = measured_peak()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank)
+    # untimed soak so that the clock samples see this load, then warm-up
+    t_end = time.perf_counter() + args.soak
+    while time.perf_counter() < t_end:
+        wl.step(stream)
+        stream.synchronize()
+    for _ in range(args.warmup):
+        wl.step(stream)
+    stream.synchronize()
+
+    nops = len(wl.names)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        wl.step(stream, ev[k])
+    stop.record(stream)
+    stop.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = wl.step_bytes * world * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    per = {}
+    for i, name in enumerate(wl.names):
+        ms = [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)]
+        avg = sum(ms) / len(ms)
+        gbs = wl.bytes[name] / (avg * 1e-3) / 1e9
+        per[name] = {"ms": avg, "ms_min": min(ms), "bytes": wl.bytes[name], "GB/s": gbs,
+                     "frac": gbs / peak, "launches": wl.launches[name]}
+    single = [n for n in per if wl.launches[n] == 1]
+    dom = max(single, key=lambda n: per[n]["ms"])
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": per[dom]["GB/s"], "peak": peak,
+                "unit": "GB/s", "frac": per[dom]["GB/s"] / peak,
+                "traffic": ncu_traffic(dom, cfg.name),
+                "algorithmic_bytes": wl.bytes[dom], "peak_source": peak_src}
+
+    e2e = None
+    if not args.no_e2e:
+        wl.pin_host()
+        n_e = max(1, min(args.e2e_steps, args.steps))
+        wl.step_e2e(stream)
+        stream.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(n_e):
+            wl.step_e2e(stream)
+        e1.record(stream)
+        e1.synchronize()
+        wall = time.perf_counter() - t0
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        e2e = {"value": wl.step_bytes * world * n_e / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes,
+               "steps": n_e, "ms_per_step": e_ms / n_e, "host_wall_ms_per_step": wall * 1e3 / n_e}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        samp = OracleSample(cfg, args.cpu_sample, host=wl.h)
+        t0 = time.perf_counter()
+        samp.step()
+        dt = time.perf_counter() - t0
+        cpu = {"value": samp.bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": samp.describe(), "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, world), "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
+            "kernels": per, "step_bytes": wl.step_bytes,
+            "peak": {"hbm_gbs": peak, "source": peak_src},
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+# ------------------------------------------------------------------ sweep
+
+def run_sweep(args):
+    import torch
+
+    import order_fem_cg_gb300 as bs
+    from order_fem_cg_gb300 import perfmodel as pm
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    peak, peak_src = measured_peak()
+    ops = {
+        "copy": (pm.bytes_copy, lambda v, a: bs.bs_copy(v[0], v[1])),
+        "axpy": (pm.bytes_axpy, lambda v, a: bs.bs_axpy(a, v[0], 1.0, v[1])),
+        "norm": (pm.bytes_norm, lambda v, a: bs.bs_norm(v[0], v[4])),
+        "dot": (pm.bytes_dot, lambda v, a: bs.bs_dot(v[0], v[1], v[4])),
+        "cg_update": (pm.bytes_cg_update,
+                      lambda v, a: bs.bs_cg_update(v[0], v[1], v[2], v[3], alpha=a, rdotr=v[4])),
+    }
+    res = {k: [] for k in ops}
+    for log2n in gen.SWEEP_LOG2:
+        x, y, alpha = gen.sweep_vectors(log2n)
+        n = x.size
+        v = [torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev),
+             torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev),
+             torch.zeros(1, dtype=torch.float64, device=dev)]
+        reps = 50 if n <= (1 << 20) else 10
+        for name, (nbytes, fn) in ops.items():
+            for _ in range(3):
+                fn(v, alpha)
+            torch.cuda.synchronize()
+            host_t, dev_t = [], []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0 = time.perf_counter()
+                e0.record(stream)
+                fn(v, alpha)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                host_t.append(time.perf_counter() - t0)
+                dev_t.append(e0.elapsed_time(e1) * 1e-3)
+            res[name].append((n, nbytes(n), statistics.median(host_t), statistics.median(dev_t)))
+        del v
+    for name, pts in res.items():
+        B = np.array([p[1] for p in pts], dtype=np.float64)
+        T = np.array([p[2] for p in pts])
+        T0, Wmax = pm.fit(B, T)
+        line = {"mode": "sweep", "op": name, "timer": "host (launch -> synchronize), median",
+                "T0_us": T0 * 1e6, "Wmax_GBs": Wmax / 1e9, "B08_bytes": pm.b_08(T0, Wmax),
+                "Wmax_frac": Wmax / 1e9 / peak, "peak_GBs": peak, "peak_source": peak_src,
+                "points": [{"n": p[0], "bytes": p[1], "host_us": p[2] * 1e6, "event_us": p[3] * 1e6,
+                            "GB/s_host": p[1] / p[2] / 1e9, "GB/s_event": p[1] / p[3] / 1e9}
+                           for p in pts]}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_probe(args):
+    import torch
+
+    import order_fem_cg_gb300 as bs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    sink = torch.zeros(1, dtype=torch.float64, device=dev)
+    ctx = bs.default_context()
+    out = []
+    for bps in (4, 8):
+        iters = 20000
+        bs.bs_probe_dfma(bps, 100, sink)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bs.bs_probe_dfma(bps, iters, sink)
+        e1.record()
+        e1.synchronize()
+        s = e0.elapsed_time(e1) * 1e-3
+        fmas = ctx.num_sms * bps * 256 * 8 * iters
+        out.append({"blocks_per_sm": bps, "dfma_per_s": fmas / s, "fp64_tflops": 2 * fmas / s / 1e12,
+                    "seconds": s, "sms": ctx.num_sms})
+    print(json.dumps({"mode": "probe", "dfma": out}), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    if args.probe:
+        return run_probe(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -30,7 +30,9 @@ builder; the tests compare the two bit for bit.
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 
 import numpy as np
 
@@ -85,10 +87,31 @@ def draws(seed: int, tag: int, n: int, start: int = 0) -> np.ndarray:
     return z
 
 
-def uniform_pm1(seed: int, tag: int, n: int) -> np.ndarray:
-    """n binary64 values uniform on (-1, 1)."""
-    k = (draws(seed, tag, n) >> np.uint64(11)).astype(np.float64)
+def _uniform_pm1_block(seed, tag, n, start):
+    k = (draws(seed, tag, n, start) >> np.uint64(11)).astype(np.float64)
     return (k * 2.0 ** -52 - 1.0) + 2.0 ** -53
+
+
+def uniform_pm1(seed: int, tag: int, n: int, threads: int = 0) -> np.ndarray:
+    """n binary64 values uniform on (-1, 1).
+
+    Large requests are drawn in blocks on a thread pool (numpy releases the
+    GIL); the values do not depend on the blocking (counter-based draws).
+    """
+    block = 1 << 22
+    if n <= block:
+        return _uniform_pm1_block(seed, tag, n, 0)
+    out = np.empty(n, dtype=np.float64)
+    starts = range(0, n, block)
+
+    def fill(a):
+        b = min(a + block, n)
+        out[a:b] = _uniform_pm1_block(seed, tag, b - a, a)
+
+    workers = threads or min(16, os.cpu_count() or 1)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(fill, starts))
+    return out
 
 
 def uniform_range(seed: int, tag: int, n: int, a: float, b: float) -> np.ndarray:

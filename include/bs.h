@@ -1,0 +1,230 @@
+/*
+ * bs.h -- C ABI of the GB300 Benchmark Streaming library (libbs.so).
+ *
+ * The seven Benchmark Streaming (BS) operations of a conjugate-gradient
+ * iteration of a high-order spectral-element solver on hexahedral meshes,
+ * in IEEE binary64 on one NVIDIA GB300 (sm_103a):
+ *
+ *   BS1 copy, BS2 AXPY, BS3 norm, BS4 inner product, BS5 fused CG update,
+ *   BS6 gather (q_G = Z^T q_L), BS7 scatter (q_L = Z q_G),
+ *
+ * as defined in "Portable high-order finite element kernels I: Streaming
+ * Operations" (the Benchmark Streaming test list; the CG vector operations;
+ * eq. (3) v_L = Z v_G; the gather/scatter kernel descriptions), plus the
+ * box-mesh index tables they run on and the sequence of one CG iteration.
+ *
+ * Conventions for every call below:
+ *  - Vectors are contiguous binary64 arrays in DEVICE memory, owned by the
+ *    caller (for instance torch tensors).  The library never allocates in
+ *    an operation call; its only device allocation is the small reduction
+ *    workspace of a context, made by bs_ctx_create.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).  Results are valid once the stream
+ *    has reached the call's position.
+ *  - Scalars a reduction produces are written to device memory (`*_dev`).
+ *  - The device current on the calling thread must be the context's device.
+ *  - Lengths are int64_t; index tables are int32_t (at most 2^31 - 1
+ *    entries).  n == 0 is a no-op, except that a reduction of length 0
+ *    writes +0.0.
+ *  - Pointers need only binary64 alignment (8 bytes).  The kernels peel a
+ *    misaligned head so that the bulk runs with 32-byte vectors; when the
+ *    operands are misaligned relative to each other a narrower vector width
+ *    is used.  BS_EALIGN is therefore never returned.
+ *  - Reductions are deterministic: for a given context (device), length
+ *    and operand alignment the result is bitwise the same on every run.
+ *  - One context serves one stream at a time: its reduction workspace is
+ *    shared by all reductions launched through it.  Use one context per
+ *    concurrently used stream.
+ *  - Return value: BS_OK (0) or a negative status; bs_strerror() names it
+ *    and bs_last_error() gives the context's last message.  On an error
+ *    nothing is launched.
+ */
+#ifndef BS_H
+#define BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define BS_OK 0
+#define BS_EINVAL (-1)  /* bad argument: NULL pointer, negative length, overlap, ... */
+#define BS_ECUDA (-2)   /* a CUDA runtime call or launch failed                     */
+#define BS_ENOMEM (-3)  /* host or context workspace allocation failed             */
+#define BS_EBOUNDS (-4) /* an index table entry is out of range (host or device)    */
+#define BS_EALIGN (-5)  /* reserved; never returned (misalignment is peeled)       */
+
+/* ---- mesh flags (bs_mesh_build_box) ------------------------------------- */
+#define BS_MESH_SHUFFLE_ELEMS 1u   /* seeded random order of elements in storage */
+#define BS_MESH_PERMUTE_GLOBAL 2u  /* seeded random global node numbering        */
+#define BS_MESH_MASK_BOUNDARY 4u   /* boundary local nodes get id -1 (masked)    */
+
+/* Largest number of CSR entries in one gather row segment the gather kernel
+ * can stage in shared memory. */
+#define BS_GATHER_SEG_MAX 4096
+/* Default target number of CSR entries per gather row segment. */
+#define BS_GATHER_SEG_DEFAULT 2048
+
+typedef struct bs_ctx bs_ctx;
+typedef struct bs_mesh bs_mesh;
+
+/* Sizes of a built mesh. */
+typedef struct {
+    int32_t E, N;        /* elements per axis, polynomial degree              */
+    uint32_t flags;      /* BS_MESH_* flags it was built with                 */
+    int32_t max_row;     /* largest number of local copies of a global node   */
+    int64_t K;           /* elements, E^3                                     */
+    int64_t NL;          /* local nodes, K (N+1)^3                            */
+    int64_t NG;          /* global nodes, (E N + 1)^3                         */
+    int64_t nnz;         /* unmasked local nodes = CSR entries of Z^T         */
+    int64_t nblocks;     /* gather row segments                               */
+    int32_t seg_max;     /* largest number of CSR entries in one segment      */
+    int32_t seg_target;  /* target entries per segment it was built with      */
+} bs_mesh_info_t;
+
+/* Device copy of a mesh's index tables, as bs_gather / bs_scatter read them.
+ * The caller uploads the four host tables of bs_mesh_tables() to device
+ * memory it owns and fills in this struct (the struct itself is host
+ * memory and is read only during the call).
+ *   scatterIds[NL]       local -> global id, -1 = masked       (BS7)
+ *   rowStarts[NG+1]      CSR row starts of Z^T, rows = global ids
+ *   localIds[nnz]        CSR column (local) ids, ascending within a row
+ *   blockStarts[nblocks+1] first row of each gather segment      (BS6) */
+typedef struct {
+    int64_t NL, NG, nnz, nblocks;
+    int32_t seg_max;
+    int32_t reserved;
+    const int32_t *scatterIds;
+    const int32_t *rowStarts;
+    const int32_t *localIds;
+    const int32_t *blockStarts;
+} bs_gs_dev;
+
+/* ---- errors -------------------------------------------------------------- */
+const char *bs_strerror(int status);
+/* Last error message recorded on `ctx` (empty string if none). */
+const char *bs_last_error(const bs_ctx *ctx);
+
+/* ---- context ------------------------------------------------------------- */
+/* Creates a context on CUDA device `device`: queries its SM count and L2
+ * size and allocates the reduction workspace (per-block partial sums, a
+ * completion counter, a device error flag), about 64 KB.  *out is owned by
+ * the caller and released by bs_ctx_destroy. */
+int bs_ctx_create(int device, bs_ctx **out);
+int bs_ctx_destroy(bs_ctx *ctx);
+/* Number of SMs of the context's device. */
+int bs_ctx_num_sms(const bs_ctx *ctx);
+/* Synchronises `stream`, then reads and clears the device error flag that
+ * the gather/scatter kernels raise on an out-of-range table entry (they
+ * skip that entry instead of touching memory out of bounds).  *out_status
+ * is BS_OK or BS_EBOUNDS. */
+int bs_ctx_device_status(bs_ctx *ctx, void *stream, int *out_status);
+
+/* ---- BS1-BS5: mesh-free vector operations ---------------------------------
+ * "Portable high-order finite element kernels I: Streaming Operations":
+ * Benchmark Streaming test list and the CG vector operations (vector
+ * addition y = alpha x + beta y, dot product alpha = x.y, norm alpha = x.x).
+ */
+
+/* BS1 copy: y[i] = x[i], i < n.  x == y is allowed; other overlap is not. */
+int bs_copy(bs_ctx *ctx, int64_t n, const double *x, double *y, void *stream);
+
+/* BS2 AXPY: y[i] = fma(alpha, x[i], beta * y[i]) with beta * y[i] rounded
+ * first (for beta == 1 that product is exact and omitted).  x == y allowed. */
+int bs_axpy(bs_ctx *ctx, int64_t n, double alpha, const double *x, double beta, double *y,
+            void *stream);
+
+/* BS3 norm: *out_dev = sum_i x[i]^2 -- the squared 2-norm, "norm:
+ * alpha = x.x"; take the square root yourself. */
+int bs_norm(bs_ctx *ctx, int64_t n, const double *x, double *out_dev, void *stream);
+
+/* BS4 inner product: *out_dev = sum_i x[i] y[i]. */
+int bs_dot(bs_ctx *ctx, int64_t n, const double *x, const double *y, double *out_dev,
+           void *stream);
+
+/* BS5 fused CG update (CG steps 8-10 fused into one pass):
+ *   x[i] = fma(alpha, p[i], x[i]);  r[i] = fma(-alpha, Ap[i], r[i]);
+ *   *rdotr_dev = sum_i r[i]^2 over the updated r.
+ * alpha is `alpha` unless both alpha_num_dev and alpha_den_dev are given,
+ * in which case alpha = *alpha_num_dev / *alpha_den_dev is formed on the
+ * device (CG's alpha = (r.r) / (p.Ap) without a host round trip).
+ * rdotr_dev may be NULL (no reduction).  x and r must not overlap each
+ * other or p, Ap. */
+int bs_cg_update(bs_ctx *ctx, int64_t n, const double *alpha_num_dev,
+                 const double *alpha_den_dev, double alpha, const double *p, const double *Ap,
+                 double *x, double *r, double *rdotr_dev, void *stream);
+
+/* ---- mesh and index tables (host) -----------------------------------------
+ * A box of E x E x E hexahedra of degree N on [0,1]^3 ("Portable high-order
+ * finite element kernels I", eq. (1): K hexahedra, (p+1)^3 GLL nodes each,
+ * N_L = K (p+1)^3).  Lattice element (ex,ey,ez) is number ex + E(ey + E ez);
+ * storage slot s holds lattice element elemPerm[s]; local node (i,j,k) of
+ * slot s has local index s (N+1)^3 + i + (N+1)(j + (N+1)k) and lies on
+ * lattice node (ex N + i, ey N + j, ez N + k), numbered x fastest on the
+ * (EN+1)^3 lattice; its global id is nodePerm[lattice number].
+ * Permutations (flags SHUFFLE_ELEMS / PERMUTE_GLOBAL, else identity): the
+ * indices 0..n-1 ordered by (z_i, i), z_i the i-th SplitMix64 output from
+ * state seed XOR (tag * 0x9E3779B97F4A7C15), tag 1 for elements, 2 for
+ * global nodes.
+ * Tables: scatterIds (local -> global, "scatterIds", negative = masked),
+ * the CSR of Z^T with rows in global-id order and each row's local ids
+ * ascending, and blockStarts grouping consecutive rows into segments of at
+ * most seg_target CSR entries (the pages' blockStarts / NODES_PER_BLOCK).
+ * Setup cost only; never timed. */
+int bs_mesh_build_box(int E, int N, uint64_t seed, uint32_t flags, bs_mesh **out);
+/* Same with an explicit segment target, 1 <= seg_target <= BS_GATHER_SEG_MAX
+ * and seg_target >= 8 (the largest row). */
+int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags, int32_t seg_target,
+                         bs_mesh **out);
+int bs_mesh_info(const bs_mesh *mesh, bs_mesh_info_t *out);
+/* Host views of the four tables, owned by the mesh (valid until destroy).
+ * Any output pointer may be NULL. */
+int bs_mesh_tables(const bs_mesh *mesh, const int32_t **scatterIds, const int32_t **rowStarts,
+                   const int32_t **localIds, const int32_t **blockStarts);
+/* Checks every table invariant (ranges, CSR consistency with scatterIds,
+ * ascending rows, segment sizes).  BS_OK, BS_EBOUNDS or BS_EINVAL. */
+int bs_mesh_validate(const bs_mesh *mesh);
+int bs_mesh_destroy(bs_mesh *mesh);
+
+/* ---- BS6 / BS7 -----------------------------------------------------------
+ * "Portable high-order finite element kernels I": the BS6 gather kernel
+ * (CSR of Z^T without values, rows blocked by blockStarts, entries staged
+ * in shared memory) and the BS7 scatter kernel (scatterIds, negative =
+ * masked); "GPU accelerated spectral finite elements on all-hex meshes":
+ * local-to-global and global-to-local tables.
+ * qL and qG must not overlap (BS_EINVAL).  Table entries out of range are
+ * skipped and raise the device error flag (see bs_ctx_device_status). */
+
+/* BS6 gather: qG[g] = (+0.0 + qL[l1]) + qL[l2] + ..., l1 < l2 < ... the
+ * local copies of global node g; a row with no entries gives +0.0. */
+int bs_gather(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double *qG, void *stream);
+
+/* BS7 scatter: qL[l] = qG[scatterIds[l]], or +0.0 where scatterIds[l] < 0. */
+int bs_scatter(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, double *qL, void *stream);
+
+/* ---- one CG iteration's streaming sequence --------------------------------
+ * With the identity as the element-local operator (S_G = Z^T S_L Z of eqs.
+ * (6)-(7) with S_L = I): pL = Z pG (BS7); ApG = Z^T pL (BS6);
+ * *pAp_dev = pG.ApG (BS4); alpha = *rr_dev / *pAp_dev;
+ * xG += alpha pG, rG -= alpha ApG, *rr_new_dev = rG.rG (BS5);
+ * *rnorm_dev = rG.rG (BS3).  pL is caller scratch of length t->NL; the
+ * other vectors have length t->NG.  Five launches on `stream`. */
+int bs_cg_iteration(bs_ctx *ctx, const bs_gs_dev *t, const double *pG, double *pL, double *ApG,
+                    double *xG, double *rG, const double *rr_dev, double *pAp_dev,
+                    double *rr_new_dev, double *rnorm_dev, void *stream);
+
+/* ---- diagnostics ----------------------------------------------------------
+ * Throughput probe of the binary64 fused multiply-add pipe: launches
+ * `blocks_per_sm` x SMs blocks of 256 threads, each thread running `iters`
+ * rounds of 8 independent fma chains (16 flops per round and chain pair),
+ * and writes a checksum to *sink_dev.  Time it with events on `stream`:
+ * DFMA/s = SMs * blocks_per_sm * 256 * 8 * iters / seconds. */
+int bs_probe_dfma(bs_ctx *ctx, int blocks_per_sm, int64_t iters, double *sink_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BS_H */

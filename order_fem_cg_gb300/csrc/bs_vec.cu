@@ -1,0 +1,595 @@
+// bs_vec.cu -- BS1-BS5: copy, AXPY, norm, inner product, fused CG update.
+//
+// "Portable high-order finite element kernels I: Streaming Operations",
+// Benchmark Streaming test list and the CG vector operations.  All five are
+// HBM streams with at most three fused multiply-adds per element, so the
+// kernels are built for bytes in flight, not arithmetic:
+//
+//  * persistent grid of (SMs x blocks-per-SM) blocks of 256 threads, grid
+//    stride over 32-byte vectors (ld/st.global.v4.f64, sm_100+), UNROLL
+//    independent vectors per operand in flight per thread;
+//  * loads skip L1 (L1::no_allocate) and ask L2 for 256-byte prefetch;
+//  * a misaligned head (< 4 elements) and the ragged tail are done by the
+//    first threads of the grid with scalar accesses;
+//  * reductions (BS3-BS5) are one launch: each block reduces its threads'
+//    fixed element sets by warp shuffles and a shared-memory step, writes
+//    one partial, and the last block to finish (completion counter, no
+//    waiting) sums the partials in a fixed tree.  The element -> thread
+//    map depends only on (grid, n, alignment), so results are bitwise
+//    reproducible run to run.  The pages' version is two kernels (a partial
+//    reduction to Nblocks values, then a second reduction) with a shuffle
+//    finish of the last warp.
+#include <cuda_runtime.h>
+
+#include "bs_internal.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int V>
+struct Vec {
+    double v[V];
+};
+
+template <int V>
+__device__ __forceinline__ Vec<V> ld_stream(const double *p);
+
+template <>
+__device__ __forceinline__ Vec<4> ld_stream<4>(const double *p)
+{
+    Vec<4> r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.f64 {%0,%1,%2,%3}, [%4];"
+                 : "=d"(r.v[0]), "=d"(r.v[1]), "=d"(r.v[2]), "=d"(r.v[3])
+                 : "l"(p));
+    return r;
+}
+
+template <>
+__device__ __forceinline__ Vec<2> ld_stream<2>(const double *p)
+{
+    Vec<2> r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v2.f64 {%0,%1}, [%2];"
+                 : "=d"(r.v[0]), "=d"(r.v[1])
+                 : "l"(p));
+    return r;
+}
+
+template <>
+__device__ __forceinline__ Vec<1> ld_stream<1>(const double *p)
+{
+    Vec<1> r;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.f64 %0, [%1];" : "=d"(r.v[0]) : "l"(p));
+    return r;
+}
+
+template <int V>
+__device__ __forceinline__ void st_stream(double *p, const Vec<V> &r);
+
+template <>
+__device__ __forceinline__ void st_stream<4>(double *p, const Vec<4> &r)
+{
+    asm volatile("st.global.L1::no_allocate.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(p), "d"(r.v[0]),
+                 "d"(r.v[1]), "d"(r.v[2]), "d"(r.v[3])
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void st_stream<2>(double *p, const Vec<2> &r)
+{
+    asm volatile("st.global.L1::no_allocate.v2.f64 [%0], {%1,%2};" ::"l"(p), "d"(r.v[0]),
+                 "d"(r.v[1])
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void st_stream<1>(double *p, const Vec<1> &r)
+{
+    asm volatile("st.global.L1::no_allocate.f64 [%0], %1;" ::"l"(p), "d"(r.v[0]) : "memory");
+}
+
+// Elements [0, h) and [h + nv V, h + nv V + t) are scalars; element index
+// of scalar slot k (k < h + t).
+__device__ __forceinline__ int64_t scalar_index(int64_t k, int64_t h, int64_t nv, int V)
+{
+    return k < h ? k : h + nv * V + (k - h);
+}
+
+struct RedOut {
+    double *partials;
+    unsigned int *counter;
+    double *out;
+};
+
+__device__ __forceinline__ double warp_sum(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide sum; the result is valid in thread 0.  Fixed order.
+__device__ __forceinline__ double block_sum(double v, double *sh)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0)
+        sh[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        v = lane < kThreads / 32 ? sh[lane] : 0.0;
+        v = warp_sum(v);
+    }
+    return v;
+}
+
+// Writes this block's partial; the last block to arrive sums all partials
+// in index order and writes the result, then re-arms the counter.
+__device__ __forceinline__ void finish_reduction(double v, const RedOut &o)
+{
+    __shared__ double sh[kThreads / 32];
+    __shared__ unsigned int ticket;
+    v = block_sum(v, sh);
+    if (threadIdx.x == 0) {
+        o.partials[blockIdx.x] = v;
+        __threadfence();
+        ticket = atomicAdd(o.counter, 1u);
+    }
+    __syncthreads();
+    if (ticket != gridDim.x - 1)
+        return;
+    __threadfence();
+    double s = 0.0;
+    for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kThreads)
+        s += __ldcg(o.partials + i);
+    s = block_sum(s, sh);
+    if (threadIdx.x == 0) {
+        *o.out = s;
+        *o.counter = 0u;
+    }
+}
+
+// ---------------------------------------------------------------- BS1 copy
+template <int V, int UNROLL>
+__global__ void __launch_bounds__(kThreads) copy_kernel(const double *__restrict__ x,
+                                                        double *__restrict__ y, int64_t h,
+                                                        int64_t nv, int64_t t)
+{
+    const int64_t gid = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const double *xv = x + h;
+    double *yv = y + h;
+    for (int64_t b = gid; b < nv; b += stride * UNROLL) {
+        Vec<V> r[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv)
+                r[u] = ld_stream<V>(xv + (b + u * stride) * V);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv)
+                st_stream<V>(yv + (b + u * stride) * V, r[u]);
+    }
+    if (gid < h + t) {
+        const int64_t i = scalar_index(gid, h, nv, V);
+        y[i] = x[i];
+    }
+}
+
+// ---------------------------------------------------------------- BS2 AXPY
+template <int V, int UNROLL, bool BETA1>
+__global__ void __launch_bounds__(kThreads) axpy_kernel(double alpha, const double *x, double beta,
+                                                        double *y, int64_t h, int64_t nv,
+                                                        int64_t t)
+{
+    const int64_t gid = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const double *xv = x + h;
+    double *yv = y + h;
+    for (int64_t b = gid; b < nv; b += stride * UNROLL) {
+        Vec<V> a[UNROLL], c[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv) {
+                a[u] = ld_stream<V>(xv + (b + u * stride) * V);
+                c[u] = ld_stream<V>(yv + (b + u * stride) * V);
+            }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv) {
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const double by = BETA1 ? c[u].v[k] : __dmul_rn(beta, c[u].v[k]);
+                    c[u].v[k] = __fma_rn(alpha, a[u].v[k], by);
+                }
+                st_stream<V>(yv + (b + u * stride) * V, c[u]);
+            }
+    }
+    if (gid < h + t) {
+        const int64_t i = scalar_index(gid, h, nv, V);
+        const double by = BETA1 ? y[i] : __dmul_rn(beta, y[i]);
+        y[i] = __fma_rn(alpha, x[i], by);
+    }
+}
+
+// ----------------------------------------------------- BS3 norm, BS4 dot
+// DOT == false: sum x_i^2 (y unused).  DOT == true: sum x_i y_i.
+template <int V, int UNROLL, bool DOT>
+__global__ void __launch_bounds__(kThreads) dot_kernel(const double *__restrict__ x,
+                                                       const double *__restrict__ y, int64_t h,
+                                                       int64_t nv, int64_t t, RedOut o)
+{
+    const int64_t gid = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const double *xv = x + h;
+    const double *yv = y + h;
+    double acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k)
+        acc[k] = 0.0;
+    for (int64_t b = gid; b < nv; b += stride * UNROLL) {
+        Vec<V> a[UNROLL], c[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv) {
+                a[u] = ld_stream<V>(xv + (b + u * stride) * V);
+                if (DOT)
+                    c[u] = ld_stream<V>(yv + (b + u * stride) * V);
+            }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv) {
+#pragma unroll
+                for (int k = 0; k < V; ++k)
+                    acc[k] = __fma_rn(a[u].v[k], DOT ? c[u].v[k] : a[u].v[k], acc[k]);
+            }
+    }
+    if (gid < h + t) {
+        const int64_t i = scalar_index(gid, h, nv, V);
+        acc[0] = __fma_rn(x[i], DOT ? y[i] : x[i], acc[0]);
+    }
+    double s = acc[0];
+#pragma unroll
+    for (int k = 1; k < V; ++k)
+        s += acc[k];
+    finish_reduction(s, o);
+}
+
+// ------------------------------------------------------ BS5 fused CG update
+template <int V, int UNROLL, bool RED>
+__global__ void __launch_bounds__(kThreads)
+    cg_kernel(const double *__restrict__ alpha_num, const double *__restrict__ alpha_den,
+              double alpha_host, const double *__restrict__ p, const double *__restrict__ Ap,
+              double *__restrict__ x, double *__restrict__ r, int64_t h, int64_t nv, int64_t t,
+              RedOut o)
+{
+    __shared__ double s_alpha;
+    double alpha = alpha_host;
+    if (alpha_num) {
+        if (threadIdx.x == 0)
+            s_alpha = __ddiv_rn(alpha_num[0], alpha_den[0]);
+        __syncthreads();
+        alpha = s_alpha;
+    }
+    const double nalpha = -alpha;
+    const int64_t gid = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    double acc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k)
+        acc[k] = 0.0;
+    for (int64_t b = gid; b < nv; b += stride * UNROLL) {
+        Vec<V> vp[UNROLL], va[UNROLL], vx[UNROLL], vr[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv) {
+                const int64_t e = h + (b + u * stride) * V;
+                vp[u] = ld_stream<V>(p + e);
+                va[u] = ld_stream<V>(Ap + e);
+                vx[u] = ld_stream<V>(x + e);
+                vr[u] = ld_stream<V>(r + e);
+            }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u)
+            if (b + u * stride < nv) {
+                const int64_t e = h + (b + u * stride) * V;
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    vx[u].v[k] = __fma_rn(alpha, vp[u].v[k], vx[u].v[k]);
+                    vr[u].v[k] = __fma_rn(nalpha, va[u].v[k], vr[u].v[k]);
+                    if (RED)
+                        acc[k] = __fma_rn(vr[u].v[k], vr[u].v[k], acc[k]);
+                }
+                st_stream<V>(x + e, vx[u]);
+                st_stream<V>(r + e, vr[u]);
+            }
+    }
+    if (gid < h + t) {
+        const int64_t i = scalar_index(gid, h, nv, V);
+        x[i] = __fma_rn(alpha, p[i], x[i]);
+        const double ri = __fma_rn(nalpha, Ap[i], r[i]);
+        r[i] = ri;
+        if (RED)
+            acc[0] = __fma_rn(ri, ri, acc[0]);
+    }
+    if (RED) {
+        double s = acc[0];
+#pragma unroll
+        for (int k = 1; k < V; ++k)
+            s += acc[k];
+        finish_reduction(s, o);
+    }
+}
+
+// ------------------------------------------------------ binary64 FMA probe
+__global__ void __launch_bounds__(kThreads) probe_dfma_kernel(int64_t iters, double *sink)
+{
+    double a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        a[k] = 1.0 + (threadIdx.x + 37 * k) * 1e-9;
+    const double m = 0.99999999, c = 1e-9;
+    for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            a[k] = __fma_rn(a[k], m, c);
+    }
+    double s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+    if (s == -1.0)  // never true; keeps the chains alive
+        *sink = s;
+}
+
+// ------------------------------------------------------------- host side
+
+// How a length-n operation over the given operands is split into a scalar
+// head, 8V-byte vectors and a scalar tail.
+struct Plan {
+    int V;
+    int64_t h, nv, t;
+};
+
+Plan make_plan(int64_t n, int vmax, const void *const *ptrs, int np)
+{
+    for (int V = vmax; V >= 2; V >>= 1) {
+        const uintptr_t bytes = 8u * V;
+        const uintptr_t m0 = reinterpret_cast<uintptr_t>(ptrs[0]) % bytes;
+        bool same = true;
+        for (int i = 1; i < np; ++i)
+            same = same && reinterpret_cast<uintptr_t>(ptrs[i]) % bytes == m0;
+        if (!same)
+            continue;
+        int64_t h = static_cast<int64_t>((bytes - m0) % bytes) / 8;
+        if (h > n)
+            h = n;
+        const int64_t nv = (n - h) / V;
+        return Plan{V, h, nv, n - h - nv * V};
+    }
+    return Plan{1, 0, n, 0};
+}
+
+bool aligned8(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 7u) == 0;
+}
+
+int grid_for(const bs_ctx *ctx, int blocks_per_sm, int64_t work_items, int cap)
+{
+    int64_t g = static_cast<int64_t>(ctx->sms) * blocks_per_sm;
+    const int64_t need = (work_items + kThreads - 1) / kThreads;
+    if (need < g)
+        g = need;
+    if (g > cap)
+        g = cap;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+
+constexpr int kStreamUnroll = 2;
+constexpr int kReduceUnroll = 2;
+constexpr int kCgUnroll = 1;
+
+template <int V>
+void launch_copy(int grid, cudaStream_t s, const double *x, double *y, const Plan &pl)
+{
+    copy_kernel<V, kStreamUnroll><<<grid, kThreads, 0, s>>>(x, y, pl.h, pl.nv, pl.t);
+}
+
+template <int V>
+void launch_axpy(int grid, cudaStream_t s, double a, const double *x, double b, double *y,
+                 const Plan &pl)
+{
+    if (b == 1.0)
+        axpy_kernel<V, kStreamUnroll, true><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv, pl.t);
+    else
+        axpy_kernel<V, kStreamUnroll, false><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv, pl.t);
+}
+
+template <int V, bool DOT>
+void launch_dot(int grid, cudaStream_t s, const double *x, const double *y, const Plan &pl,
+                const RedOut &o)
+{
+    dot_kernel<V, kReduceUnroll, DOT><<<grid, kThreads, 0, s>>>(x, y, pl.h, pl.nv, pl.t, o);
+}
+
+template <int V>
+void launch_cg(int grid, cudaStream_t s, const double *num, const double *den, double alpha,
+               const double *p, const double *Ap, double *x, double *r, const Plan &pl,
+               const RedOut &o, bool red)
+{
+    if (red)
+        cg_kernel<V, kCgUnroll, true><<<grid, kThreads, 0, s>>>(num, den, alpha, p, Ap, x, r, pl.h,
+                                                                pl.nv, pl.t, o);
+    else
+        cg_kernel<V, kCgUnroll, false><<<grid, kThreads, 0, s>>>(num, den, alpha, p, Ap, x, r,
+                                                                 pl.h, pl.nv, pl.t, o);
+}
+
+int reduce_grid(const bs_ctx *ctx, const Plan &pl, int unroll)
+{
+    return grid_for(ctx, ctx->tune.reduce_blocks_per_sm, (pl.nv + unroll - 1) / unroll,
+                    kMaxReduceBlocks);
+}
+
+} // namespace
+
+extern "C" int bs_copy(bs_ctx *ctx, int64_t n, const double *x, double *y, void *stream)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (n < 0 || (n > 0 && (!x || !y)))
+        return bs_set_error(ctx, BS_EINVAL, "bs_copy: bad length or NULL pointer");
+    if (n == 0)
+        return BS_OK;
+    if (!aligned8(x) || !aligned8(y))
+        return bs_set_error(ctx, BS_EINVAL, "bs_copy: pointers must be 8-byte aligned");
+    if (x != y && bs_overlap(x, 8 * n, y, 8 * n))
+        return bs_set_error(ctx, BS_EINVAL, "bs_copy: x and y overlap");
+    if (int st = bs_check_device(ctx))
+        return st;
+    if (x == y)
+        return BS_OK;
+    const void *ps[2] = {x, y};
+    const Plan pl = make_plan(n, ctx->tune.vec_width, ps, 2);
+    const int grid = grid_for(ctx, ctx->tune.stream_blocks_per_sm, (pl.nv + 1) / 2, 1 << 30);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (pl.V) {
+    case 4: launch_copy<4>(grid, s, x, y, pl); break;
+    case 2: launch_copy<2>(grid, s, x, y, pl); break;
+    default: launch_copy<1>(grid, s, x, y, pl); break;
+    }
+    BS_LAUNCH_CHECK(ctx, "copy_kernel");
+    return BS_OK;
+}
+
+extern "C" int bs_axpy(bs_ctx *ctx, int64_t n, double alpha, const double *x, double beta,
+                       double *y, void *stream)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (n < 0 || (n > 0 && (!x || !y)))
+        return bs_set_error(ctx, BS_EINVAL, "bs_axpy: bad length or NULL pointer");
+    if (n == 0)
+        return BS_OK;
+    if (!aligned8(x) || !aligned8(y))
+        return bs_set_error(ctx, BS_EINVAL, "bs_axpy: pointers must be 8-byte aligned");
+    if (x != y && bs_overlap(x, 8 * n, y, 8 * n))
+        return bs_set_error(ctx, BS_EINVAL, "bs_axpy: x and y overlap");
+    if (int st = bs_check_device(ctx))
+        return st;
+    const void *ps[2] = {x, y};
+    const Plan pl = make_plan(n, ctx->tune.vec_width, ps, 2);
+    const int grid = grid_for(ctx, ctx->tune.stream_blocks_per_sm, (pl.nv + 1) / 2, 1 << 30);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (pl.V) {
+    case 4: launch_axpy<4>(grid, s, alpha, x, beta, y, pl); break;
+    case 2: launch_axpy<2>(grid, s, alpha, x, beta, y, pl); break;
+    default: launch_axpy<1>(grid, s, alpha, x, beta, y, pl); break;
+    }
+    BS_LAUNCH_CHECK(ctx, "axpy_kernel");
+    return BS_OK;
+}
+
+static int dot_common(bs_ctx *ctx, const char *name, int64_t n, const double *x, const double *y,
+                      double *out, void *stream, bool dot)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (n < 0 || !out || (n > 0 && (!x || (dot && !y))))
+        return bs_set_error(ctx, BS_EINVAL, "%s: bad length or NULL pointer", name);
+    if (!aligned8(out) || (n > 0 && (!aligned8(x) || (dot && !aligned8(y)))))
+        return bs_set_error(ctx, BS_EINVAL, "%s: pointers must be 8-byte aligned", name);
+    if (int st = bs_check_device(ctx))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        BS_CUDA_TRY(ctx, cudaMemsetAsync(out, 0, sizeof(double), s));
+        return BS_OK;
+    }
+    const void *ps[2] = {x, dot ? y : x};
+    const Plan pl = make_plan(n, ctx->tune.vec_width, ps, 2);
+    const int grid = reduce_grid(ctx, pl, kReduceUnroll);
+    const RedOut o{ctx->partials, ctx->counter, out};
+    if (dot) {
+        switch (pl.V) {
+        case 4: launch_dot<4, true>(grid, s, x, y, pl, o); break;
+        case 2: launch_dot<2, true>(grid, s, x, y, pl, o); break;
+        default: launch_dot<1, true>(grid, s, x, y, pl, o); break;
+        }
+    } else {
+        switch (pl.V) {
+        case 4: launch_dot<4, false>(grid, s, x, x, pl, o); break;
+        case 2: launch_dot<2, false>(grid, s, x, x, pl, o); break;
+        default: launch_dot<1, false>(grid, s, x, x, pl, o); break;
+        }
+    }
+    BS_LAUNCH_CHECK(ctx, name);
+    return BS_OK;
+}
+
+extern "C" int bs_norm(bs_ctx *ctx, int64_t n, const double *x, double *out_dev, void *stream)
+{
+    return dot_common(ctx, "bs_norm", n, x, nullptr, out_dev, stream, false);
+}
+
+extern "C" int bs_dot(bs_ctx *ctx, int64_t n, const double *x, const double *y, double *out_dev,
+                      void *stream)
+{
+    return dot_common(ctx, "bs_dot", n, x, y, out_dev, stream, true);
+}
+
+extern "C" int bs_cg_update(bs_ctx *ctx, int64_t n, const double *alpha_num_dev,
+                            const double *alpha_den_dev, double alpha, const double *p,
+                            const double *Ap, double *x, double *r, double *rdotr_dev,
+                            void *stream)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (n < 0 || (n > 0 && (!p || !Ap || !x || !r)))
+        return bs_set_error(ctx, BS_EINVAL, "bs_cg_update: bad length or NULL pointer");
+    if ((alpha_num_dev == nullptr) != (alpha_den_dev == nullptr))
+        return bs_set_error(ctx, BS_EINVAL,
+                            "bs_cg_update: give both alpha_num_dev and alpha_den_dev or neither");
+    if ((rdotr_dev && !aligned8(rdotr_dev)) || (alpha_num_dev && !aligned8(alpha_num_dev)) ||
+        (alpha_den_dev && !aligned8(alpha_den_dev)) ||
+        (n > 0 && (!aligned8(p) || !aligned8(Ap) || !aligned8(x) || !aligned8(r))))
+        return bs_set_error(ctx, BS_EINVAL, "bs_cg_update: pointers must be 8-byte aligned");
+    const int64_t nb = 8 * n;
+    if (bs_overlap(x, nb, r, nb) || bs_overlap(x, nb, p, nb) || bs_overlap(x, nb, Ap, nb) ||
+        bs_overlap(r, nb, p, nb) || bs_overlap(r, nb, Ap, nb))
+        return bs_set_error(ctx, BS_EINVAL, "bs_cg_update: x and r must not overlap x, r, p, Ap");
+    if (int st = bs_check_device(ctx))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        if (rdotr_dev)
+            BS_CUDA_TRY(ctx, cudaMemsetAsync(rdotr_dev, 0, sizeof(double), s));
+        return BS_OK;
+    }
+    const void *ps[4] = {p, Ap, x, r};
+    const Plan pl = make_plan(n, ctx->tune.vec_width, ps, 4);
+    const int grid = reduce_grid(ctx, pl, kCgUnroll);
+    const RedOut o{ctx->partials, ctx->counter, rdotr_dev};
+    const bool red = rdotr_dev != nullptr;
+    switch (pl.V) {
+    case 4: launch_cg<4>(grid, s, alpha_num_dev, alpha_den_dev, alpha, p, Ap, x, r, pl, o, red); break;
+    case 2: launch_cg<2>(grid, s, alpha_num_dev, alpha_den_dev, alpha, p, Ap, x, r, pl, o, red); break;
+    default: launch_cg<1>(grid, s, alpha_num_dev, alpha_den_dev, alpha, p, Ap, x, r, pl, o, red); break;
+    }
+    BS_LAUNCH_CHECK(ctx, "cg_kernel");
+    return BS_OK;
+}
+
+extern "C" int bs_probe_dfma(bs_ctx *ctx, int blocks_per_sm, int64_t iters, double *sink_dev,
+                             void *stream)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (blocks_per_sm < 1 || blocks_per_sm > 64 || iters < 0 || !sink_dev)
+        return bs_set_error(ctx, BS_EINVAL, "bs_probe_dfma: bad argument");
+    if (int st = bs_check_device(ctx))
+        return st;
+    probe_dfma_kernel<<<ctx->sms * blocks_per_sm, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        iters, sink_dev);
+    BS_LAUNCH_CHECK(ctx, "probe_dfma_kernel");
+    return BS_OK;
+}

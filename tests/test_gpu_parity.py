@@ -1,0 +1,310 @@
+"""GPU parity: the sm_103a kernels through the C ABI against the CPU oracle.
+
+Tolerances: copy, AXPY, the fused update's x and r, scatter and gather are
+bit-exact; norm, dot and the fused residual r.r are within 1e-12 relative
+of the oracle's Dot2 value (the reductions sum in a different order), and
+every reduction is bitwise reproducible run to run.
+"""
+
+import numpy as np
+import pytest
+
+import bsinputs as gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from order_fem_cg_gb300 import build as _build  # noqa: E402
+
+_build.build()
+import order_fem_cg_gb300 as bs  # noqa: E402
+
+DEV = torch.device("cuda", 0)
+RTOL_RED = 1e-12
+
+SIZES = [0, 1, 2, 3, 4, 5, 7, 31, 257, 1000, 4099, 65536 + 3, 1000003]
+OFFSETS = [(0, 0), (1, 1), (2, 2), (3, 3), (1, 0), (0, 2), (2, 3)]
+
+
+def dev(a, offset=0):
+    """Device copy of a at element offset `offset` inside a larger buffer (misaligned views)."""
+    buf = torch.empty(a.size + offset + 1, dtype=torch.float64, device=DEV)
+    v = buf[offset:offset + a.size]
+    v.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return v
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def bits_equal(a, b):
+    return np.array_equal(np.asarray(a).view(np.uint64), np.asarray(b).view(np.uint64))
+
+
+def rel_close(got, ref, rtol=RTOL_RED):
+    return abs(got - ref) <= rtol * abs(ref) or (ref == 0.0 and got == 0.0)
+
+
+@pytest.mark.parametrize("n", SIZES)
+@pytest.mark.parametrize("off", OFFSETS)
+def test_copy(n, off):
+    x = gen.uniform_pm1(1, 7, n)
+    xd, yd = dev(x, off[0]), dev(np.zeros(n), off[1])
+    bs.bs_copy(xd, yd)
+    assert bits_equal(host(yd), oracle.copy(x))
+
+
+@pytest.mark.parametrize("beta", [1.0, -0.5, 0.3])
+@pytest.mark.parametrize("n", [0, 1, 5, 1000, 65536 + 3, 1000003])
+@pytest.mark.parametrize("off", [(0, 0), (3, 3), (1, 2)])
+def test_axpy(beta, n, off):
+    x = gen.uniform_pm1(2, 7, n)
+    y = gen.uniform_pm1(2, 9, n)
+    xd, yd = dev(x, off[0]), dev(y, off[1])
+    bs.bs_axpy(0.37, xd, beta, yd)
+    assert bits_equal(host(yd), oracle.axpy(0.37, x, beta, y))
+
+
+def test_axpy_aliased():
+    x = gen.uniform_pm1(3, 7, 100003)
+    xd = dev(x, 1)
+    bs.bs_axpy(0.37, xd, 1.0, xd)
+    assert bits_equal(host(xd), oracle.axpy(0.37, x, 1.0, x))
+
+
+@pytest.mark.parametrize("n", SIZES + [1 << 22])
+@pytest.mark.parametrize("off", [(0, 0), (1, 1), (3, 3), (1, 2)])
+def test_norm_and_dot(n, off):
+    x = gen.uniform_pm1(4, 7, n)
+    y = gen.uniform_pm1(4, 9, n)
+    xd, yd = dev(x, off[0]), dev(y, off[1])
+    nr = host(bs.bs_norm(xd))[0]
+    dt = host(bs.bs_dot(xd, yd))[0]
+    assert rel_close(nr, oracle.norm(x))
+    assert rel_close(dt, oracle.dot(x, y))
+    # run to run: bitwise identical
+    assert bits_equal(host(bs.bs_norm(xd)), [nr])
+    assert bits_equal(host(bs.bs_dot(xd, yd)), [dt])
+    if n == 0:
+        assert not np.signbit(nr) and not np.signbit(dt)
+
+
+def test_norm_closed_forms():
+    n = 1000003
+    assert host(bs.bs_norm(dev(np.full(n, 0.5))))[0] == n / 4
+    i = np.arange(n, dtype=np.float64)
+    exact = (n - 1) * n * (2 * n - 1) // 6
+    assert abs(host(bs.bs_norm(dev(i)))[0] - exact) <= 1e-12 * exact
+    assert host(bs.bs_dot(dev(i), dev(np.ones(n))))[0] == n * (n - 1) // 2
+
+
+@pytest.mark.parametrize("log2n", [10, 17, 27])
+def test_sweep_points(log2n):
+    x, y, alpha = gen.sweep_vectors(log2n)
+    xd, yd = dev(x), dev(y)
+    assert rel_close(host(bs.bs_norm(xd))[0], oracle.norm(x))
+    assert rel_close(host(bs.bs_dot(xd, yd))[0], oracle.dot(x, y))
+    bs.bs_axpy(alpha, xd, 1.0, yd)
+    assert bits_equal(host(yd), oracle.axpy(alpha, x, 1.0, y))
+    zd = dev(np.zeros(x.size))
+    bs.bs_copy(xd, zd)
+    assert bits_equal(host(zd), x)
+
+
+@pytest.mark.parametrize("n", [0, 1, 3, 6, 1000, 65536 + 3, 1000003])
+@pytest.mark.parametrize("off", [(0, 0, 0, 0), (1, 1, 1, 1), (0, 1, 2, 3)])
+def test_cg_update(n, off):
+    p, Ap, x, r = (gen.uniform_pm1(5, t, n) for t in (gen.TAG_P, gen.TAG_AP, gen.TAG_X, gen.TAG_R))
+    alpha = 0.37
+    pd, Apd, xd, rd = dev(p, off[0]), dev(Ap, off[1]), dev(x, off[2]), dev(r, off[3])
+    rr = host(bs.bs_cg_update(pd, Apd, xd, rd, alpha=alpha))[0]
+    xo, ro, rro = oracle.cg_update(alpha, p, Ap, x, r)
+    assert bits_equal(host(xd), xo) and bits_equal(host(rd), ro)
+    assert rel_close(rr, rro)
+    assert rel_close(rr, oracle.norm(host(rd)))
+
+
+def test_cg_update_device_alpha_and_no_reduction():
+    n = 300007
+    p, Ap, x, r = (gen.uniform_pm1(6, t, n) for t in (4, 5, 7, 6))
+    num = torch.tensor([0.8], dtype=torch.float64, device=DEV)
+    den = torch.tensor([3.0], dtype=torch.float64, device=DEV)
+    alpha = 0.8 / 3.0
+    pd, Apd, xd, rd = dev(p), dev(Ap), dev(x), dev(r)
+    rr = host(bs.bs_cg_update(pd, Apd, xd, rd, alpha_num=num, alpha_den=den))[0]
+    xo, ro, rro = oracle.cg_update(alpha, p, Ap, x, r)
+    assert bits_equal(host(xd), xo) and bits_equal(host(rd), ro) and rel_close(rr, rro)
+    pd, Apd, xd, rd = dev(p), dev(Ap), dev(x), dev(r)
+    assert bs.bs_cg_update(pd, Apd, xd, rd, alpha=alpha, reduce=False) is None
+    assert bits_equal(host(xd), xo) and bits_equal(host(rd), ro)
+
+
+def test_reductions_bitwise_reproducible_large():
+    n = (1 << 25) + 12345
+    x = gen.normal(7, 3, n)
+    xd = dev(x, 1)
+    vals = {host(bs.bs_norm(xd)).view(np.uint64)[0] for _ in range(5)}
+    assert len(vals) == 1
+
+
+# ------------------------------------------------------------- meshes
+
+def mesh_case(cfg, seg=None):
+    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags, seg_target=seg)
+    assert m.validate() == bs.BS_OK
+    ids = m.tables()["scatterIds"]
+    ep, npm = gen.mesh_perms(cfg)
+    ids_o = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+    assert np.array_equal(ids, ids_o)
+    return m, m.to_device(0), ids_o
+
+
+MESHES = [
+    (gen.CONFIGS["tiny"], None),
+    (gen.CONFIGS["tiny"], 8),
+    (gen.CONFIGS["tiny"], 1000),
+    (gen.CONFIGS["tiny"], 4096),
+    (gen.MeshConfig("masked", 6, 4, 17, 7), None),
+    (gen.MeshConfig("plain", 5, 2, 3, 0), 3000),
+    (gen.MeshConfig("one", 1, 1, 5, 3), None),
+    (gen.MeshConfig("onemask", 1, 3, 5, 7), 8),
+    (gen.CONFIGS["mid"], None),
+]
+
+
+@pytest.mark.parametrize("cfg,seg", MESHES, ids=lambda v: getattr(v, "name", str(v)))
+def test_scatter_gather(cfg, seg):
+    m, t, ids = mesh_case(cfg, seg)
+    qG = gen.uniform_pm1(cfg.seed, gen.TAG_U, cfg.NG)
+    qL = gen.uniform_pm1(cfg.seed, gen.TAG_P, cfg.NL)
+    qLd = dev(np.zeros(cfg.NL))
+    bs.bs_scatter(t, dev(qG), qLd)
+    assert bits_equal(host(qLd), oracle.scatter(ids, qG))
+    qGd = dev(np.full(cfg.NG, np.nan))
+    bs.bs_gather(t, dev(qL), qGd)
+    assert bits_equal(host(qGd), oracle.gather(ids, qL, cfg.NG))
+    assert bs.default_context().device_status() == bs.BS_OK
+
+
+def test_scatter_unaligned_views():
+    cfg = gen.CONFIGS["tiny"]
+    m, t, ids = mesh_case(cfg)
+    qG = gen.uniform_pm1(1, 1, cfg.NG)
+    qLd = dev(np.zeros(cfg.NL), 1)            # 8-byte aligned only: scalar path
+    bs.bs_scatter(t, dev(qG, 3), qLd)
+    assert bits_equal(host(qLd), oracle.scatter(ids, qG))
+
+
+def test_gather_sum_order_probe():
+    """Rows whose sum depends on order: 1.0 at the smallest local id, 2^-53 elsewhere."""
+    cfg = gen.CONFIGS["tiny"]
+    m, t, ids = mesh_case(cfg)
+    tabs = m.tables()
+    rs, li = tabs["rowStarts"], tabs["localIds"]
+    for first in (True, False):
+        qL = np.full(cfg.NL, 2.0 ** -53)
+        pick = rs[:-1] if first else rs[1:] - 1
+        qL[li[pick]] = 1.0
+        qGd = dev(np.zeros(cfg.NG))
+        bs.bs_gather(t, dev(qL), qGd)
+        assert bits_equal(host(qGd), oracle.gather(ids, qL, cfg.NG))
+
+
+def test_gather_of_ones_and_identities():
+    cfg = gen.CONFIGS["mid"]
+    m, t, ids = mesh_case(cfg)
+    mult = dev(np.zeros(cfg.NG))
+    bs.bs_gather(t, dev(np.ones(cfg.NL)), mult)
+    mh = host(mult)
+    a, b = cfg.E - 1, cfg.E * (cfg.N - 1) + 2
+    vals, counts = np.unique(mh, return_counts=True)
+    assert dict(zip(vals.astype(int).tolist(), counts.tolist())) == {
+        1: b ** 3, 2: 3 * a * b * b, 4: 3 * a * a * b, 8: a ** 3}
+    u = gen.integers_dyadic(cfg.seed, 3, cfg.NG)
+    qL = dev(np.zeros(cfg.NL))
+    bs.bs_scatter(t, dev(u), qL)
+    back = dev(np.zeros(cfg.NG))
+    bs.bs_gather(t, qL, back)
+    assert np.array_equal(host(back), mh * u)
+
+
+def test_out_of_range_entry_is_flagged_not_dereferenced():
+    cfg = gen.CONFIGS["tiny"]
+    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    tabs = m.tables()
+    bad_ids = tabs["scatterIds"].copy()
+    bad_ids[123] = cfg.NG + 5               # beyond q_G: the kernel must skip it
+    bad_local = tabs["localIds"].copy()
+    bad_local[77] = cfg.NL + 1000           # beyond q_L
+    tabs_bad = dict(tabs, scatterIds=bad_ids, localIds=bad_local)
+    t = bs.DeviceTables.from_host(tabs_bad, m.info, 0)
+    ctx = bs.default_context()
+    assert ctx.device_status() == bs.BS_OK
+    qG = gen.uniform_pm1(1, 1, cfg.NG)
+    qLd = dev(np.zeros(cfg.NL))
+    bs.bs_scatter(t, dev(qG), qLd)
+    assert ctx.device_status() == bs.BS_EBOUNDS
+    got = host(qLd)
+    assert got[123] == 0.0
+    good = np.ones(cfg.NL, bool)
+    good[123] = False
+    assert bits_equal(got[good], oracle.scatter(tabs["scatterIds"], qG)[good])
+    qGd = dev(np.zeros(cfg.NG))
+    bs.bs_gather(t, dev(gen.uniform_pm1(1, 2, cfg.NL)), qGd)
+    assert ctx.device_status() == bs.BS_EBOUNDS
+    assert ctx.device_status() == bs.BS_OK   # the flag was cleared by the read
+
+
+def test_invalid_arguments_rejected():
+    x = dev(np.zeros(10))
+    with pytest.raises(ValueError):
+        bs.bs_copy(x, x[:9])
+    with pytest.raises(bs.BSError):
+        bs.bs_copy(x[0:6], x[4:10])            # partial overlap
+    cfg = gen.CONFIGS["tiny"]
+    m, t, ids = mesh_case(cfg)
+    buf = torch.zeros(cfg.NL, dtype=torch.float64, device=DEV)
+    with pytest.raises(bs.BSError):
+        bs.bs_gather(t, buf, buf[:cfg.NG])     # qL and qG overlap
+    p = dev(np.zeros(100))
+    with pytest.raises(bs.BSError):
+        bs.bs_cg_update(p, p, p, p, alpha=1.0)
+
+
+# ---------------------------------------------------------- CG sequence
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_cg_iteration_sequence(name):
+    cfg = gen.CONFIGS[name]
+    m, t, ids = mesh_case(cfg)
+    NG = cfg.NG
+    pG = gen.uniform_pm1(cfg.seed, gen.TAG_P, NG)
+    xG = gen.uniform_pm1(cfg.seed, gen.TAG_X, NG)
+    rG = gen.uniform_pm1(cfg.seed, gen.TAG_R, NG)
+    rr = oracle.norm(rG)
+    ref = oracle.cg_sequence(ids, pG, xG, rG, rr)
+    pGd, xGd, rGd = dev(pG), dev(xG), dev(rG)
+    pLd, ApGd = dev(np.zeros(cfg.NL)), dev(np.zeros(NG))
+    sc = {k: torch.zeros(1, dtype=torch.float64, device=DEV) for k in ("pAp", "rr_new", "rnorm")}
+    rrd = torch.tensor([rr], dtype=torch.float64, device=DEV)
+    bs.bs_cg_iteration(t, pGd, pLd, ApGd, xGd, rGd, rrd, sc["pAp"], sc["rr_new"], sc["rnorm"])
+    assert bits_equal(host(pLd), ref["pL"]) and bits_equal(host(ApGd), ref["ApG"])
+    pAp = host(sc["pAp"])[0]
+    assert rel_close(pAp, ref["pAp"])
+    alpha = rr / pAp
+    # x, r depend on alpha = rr / pAp, whose last bits follow the reduction
+    # order: |dx| <= |d alpha| |p| + 1 ulp, |d alpha| <= 2e-12 |alpha|.
+    da = 2e-12 * abs(ref["alpha"])
+    for got, exp, v in ((host(xGd), ref["x"], pG), (host(rGd), ref["r"], host(ApGd))):
+        assert np.all(np.abs(got - exp) <= da * np.abs(v) + np.spacing(np.abs(exp)))
+    assert rel_close(host(sc["rr_new"])[0], ref["rr_new"], 1e-11)
+    assert rel_close(host(sc["rnorm"])[0], oracle.norm(host(rGd)))
+    assert bits_equal(host(sc["rnorm"]), host(sc["rr_new"])) or rel_close(
+        host(sc["rnorm"])[0], host(sc["rr_new"])[0])
+    assert abs(alpha - ref["alpha"]) <= da
