@@ -109,7 +109,7 @@ def _declare(lib):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is not built: run `python -m order_fem_cg_gb300.build` "
+            f"{LIB_PATH} is not built: run `python order_fem_cg_gb300/build.py` "
             "(nvcc for sm_103a); there is no non-CUDA implementation")
     lib = ctypes.CDLL(LIB_PATH)
     _declare(lib)

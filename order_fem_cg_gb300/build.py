@@ -2,7 +2,8 @@
 
 Four translation units are compiled in parallel and linked with the static
 CUDA runtime, so the library needs only the driver (libcuda) at run time.
-Run as ``python -m order_fem_cg_gb300.build``.
+Run as ``python order_fem_cg_gb300/build.py`` (it does not import the package,
+whose import needs the library built here).
 """
 
 from __future__ import annotations

@@ -10,6 +10,17 @@ if ROOT not in sys.path:
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 
+def build_lib():
+    """Build libbs.so (if stale) without importing the package first."""
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location(
+        "_bs_libbuild", os.path.join(ROOT, "order_fem_cg_gb300", "build.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
 

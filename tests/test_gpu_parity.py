@@ -18,9 +18,9 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
-from order_fem_cg_gb300 import build as _build  # noqa: E402
+from conftest import build_lib  # noqa: E402
 
-_build.build()
+build_lib()
 import order_fem_cg_gb300 as bs  # noqa: E402
 
 DEV = torch.device("cuda", 0)

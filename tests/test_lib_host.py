@@ -9,13 +9,12 @@ import pytest
 
 import bsinputs as gen
 import oracle
-from conftest import ROOT
+from conftest import ROOT, build_lib
 
 
 @pytest.fixture(scope="module")
 def bs():
-    from order_fem_cg_gb300 import build
-    build.build()
+    build_lib()
     import order_fem_cg_gb300 as bs
     return bs
 
