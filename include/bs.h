@@ -223,6 +223,30 @@ int bs_cg_iteration(bs_ctx *ctx, const bs_gs_dev *t, const double *pG, double *p
  * DFMA/s = SMs * blocks_per_sm * 256 * 8 * iters / seconds. */
 int bs_probe_dfma(bs_ctx *ctx, int blocks_per_sm, int64_t iters, double *sink_dev, void *stream);
 
+/* ---- allocation-free inner product ----------------------------------------
+ * The paper has no counterpart to this entry point; it is a library
+ * convenience.  For callers that cannot call cudaMalloc -- code running
+ * inside a device-memory allocator's hooks or a host callback, or an
+ * embedding runtime that owns every device allocation -- and therefore
+ * cannot create a bs_ctx (a context allocates its reduction workspace).
+ *
+ * Computes *out_dev = sum_i x[i] y[i] like bs_dot, with the same kernel,
+ * but keeps the per-block partial sums and the completion counter in one
+ * static device array of 8,448 bytes (1,024 partial sums plus the
+ * counter) that every GPU loading this library holds until the process
+ * exits.  It calls no cudaMalloc, cudaFree or allocating library routine.
+ *  - Uses the calling thread's current device.  The first call on a device
+ *    looks up the array's device address (cudaGetSymbolAddress) and the SM
+ *    count; make that first call before any stream capture.
+ *  - Each call first clears the counter on `stream` (the array keeps the
+ *    previous call's contents).  All calls share the one array, so calls
+ *    whose work overlaps on the GPU (other streams, other threads) race and
+ *    give wrong results: serialise them.
+ *  - BS_EINVAL if the device would need more than 1,024 partial sums
+ *    (more than 256 SMs) or on a bad argument; BS_ECUDA on a CUDA error.
+ *    There is no context, so there is no error message beyond the code. */
+int bs_dot_noalloc(int64_t n, const double *x, const double *y, double *out_dev, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

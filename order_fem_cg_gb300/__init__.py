@@ -43,7 +43,7 @@ EXPORTS = (
     "bs_ctx_device_status", "bs_copy", "bs_axpy", "bs_norm", "bs_dot", "bs_cg_update",
     "bs_mesh_build_box", "bs_mesh_build_box_ex", "bs_mesh_info", "bs_mesh_tables",
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
-    "bs_probe_dfma",
+    "bs_probe_dfma", "bs_dot_noalloc",
 )
 
 
@@ -99,6 +99,7 @@ def _declare(lib):
         "bs_scatter": ([_vp, ctypes.POINTER(GSDev), _vp, _vp, _vp], _int),
         "bs_cg_iteration": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 10, _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
+        "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -259,6 +260,19 @@ def bs_cg_update(p, Ap, x, r, alpha=0.0, alpha_num=None, alpha_den=None, rdotr=N
                                _vp(rdotr.data_ptr()) if reduce else _vp(0), _stream(stream)),
               "bs_cg_update")
     return rdotr if reduce else None
+
+
+def bs_dot_noalloc(x, y, out, stream=None):
+    """BS4 without a context: for callers that cannot allocate device memory.
+
+    Same result as bs_dot, with the reduction's scratch in a static device
+    array shared by all calls (serialise calls; `out` must be preallocated).
+    """
+    st = lib.bs_dot_noalloc(x.numel(), _vec(x, "x"), _vec(y, "y", x.numel()), _vec(out, "out", 1),
+                            _stream(stream))
+    if st != BS_OK:
+        raise BSError(st, "bs_dot_noalloc")
+    return out
 
 
 def bs_probe_dfma(blocks_per_sm, iters, sink, stream=None, ctx=None):

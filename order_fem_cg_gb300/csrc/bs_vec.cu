@@ -21,6 +21,8 @@
 //    finish of the last warp.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "bs_internal.h"
 
 namespace {
@@ -592,4 +594,94 @@ extern "C" int bs_probe_dfma(bs_ctx *ctx, int blocks_per_sm, int64_t iters, doub
         iters, sink_dev);
     BS_LAUNCH_CHECK(ctx, "probe_dfma_kernel");
     return BS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free inner product.
+//
+// Some callers cannot call cudaMalloc: code that runs inside a memory
+// allocator's own hooks, a host callback, or an embedding runtime that owns
+// every device allocation and forbids others.  They cannot create a bs_ctx
+// either, since a context allocates its reduction workspace.  bs_dot_noalloc
+// runs the same BS4 kernel as bs_dot but keeps the per-block partial sums
+// and the completion counter in the fixed array below, which every GPU that
+// loads this library holds until the process exits.
+namespace {
+constexpr int kNoAllocMaxBlocks = 1024;  // partial sums the array can hold
+constexpr size_t kNoAllocCounterOffset = kNoAllocMaxBlocks * sizeof(double);
+constexpr size_t kNoAllocScratchBytes = kNoAllocCounterOffset + 256;
+constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocBlocksPerSm = 4;
+} // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+int g_noalloc_sms[kNoAllocMaxDevices];
+
+// Device address of the scratch array and the SM count of the current
+// device, looked up once per device (the first call on a device does it).
+int noalloc_setup(int *dev_out, unsigned char **scratch, int *sms)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return BS_ECUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        int n_sms = 0;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
+            cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return BS_ECUDA;
+        }
+        g_noalloc_sms[dev] = n_sms;
+        g_noalloc_addr[dev] = p;
+    }
+    *dev_out = dev;
+    *scratch = static_cast<unsigned char *>(g_noalloc_addr[dev]);
+    *sms = g_noalloc_sms[dev];
+    return BS_OK;
+}
+
+} // namespace
+
+extern "C" int bs_dot_noalloc(int64_t n, const double *x, const double *y, double *out_dev,
+                              void *stream)
+{
+    if (n < 0 || !out_dev || (n > 0 && (!x || !y)))
+        return BS_EINVAL;
+    if (!aligned8(out_dev) || (n > 0 && (!aligned8(x) || !aligned8(y))))
+        return BS_EINVAL;
+    int dev = 0, sms = 0;
+    unsigned char *scratch = nullptr;
+    if (int st = noalloc_setup(&dev, &scratch, &sms))
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (n == 0)
+        return cudaMemsetAsync(out_dev, 0, sizeof(double), s) == cudaSuccess ? BS_OK : BS_ECUDA;
+    const void *ps[2] = {x, y};
+    const Plan pl = make_plan(n, 4, ps, 2);
+    const int64_t need = ((pl.nv + kReduceUnroll - 1) / kReduceUnroll + kThreads - 1) / kThreads;
+    int64_t grid = static_cast<int64_t>(sms) * kNoAllocBlocksPerSm;
+    if (need < grid)
+        grid = need < 1 ? 1 : need;
+    if (grid > kNoAllocMaxBlocks)
+        return BS_EINVAL;  // the device wants more partial sums than the array holds
+    unsigned int *counter = reinterpret_cast<unsigned int *>(scratch + kNoAllocCounterOffset);
+    // The array keeps the previous call's contents; the counter must start at 0.
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess)
+        return BS_ECUDA;
+    const RedOut o{reinterpret_cast<double *>(scratch), counter, out_dev};
+    switch (pl.V) {
+    case 4: launch_dot<4, true>(static_cast<int>(grid), s, x, y, pl, o); break;
+    case 2: launch_dot<2, true>(static_cast<int>(grid), s, x, y, pl, o); break;
+    default: launch_dot<1, true>(static_cast<int>(grid), s, x, y, pl, o); break;
+    }
+    return cudaGetLastError() == cudaSuccess ? BS_OK : BS_ECUDA;
 }
