@@ -43,7 +43,7 @@ EXPORTS = (
     "bs_ctx_device_status", "bs_copy", "bs_axpy", "bs_norm", "bs_dot", "bs_cg_update",
     "bs_mesh_build_box", "bs_mesh_build_box_ex", "bs_mesh_info", "bs_mesh_tables",
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
-    "bs_probe_dfma", "bs_dot_noalloc",
+    "bs_probe_dfma", "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
 )
 
 
@@ -60,12 +60,32 @@ class MeshInfo(ctypes.Structure):
                 ("seg_max", ctypes.c_int32), ("seg_target", ctypes.c_int32)]
 
 
+_PLAN_INTS = ("s_ntiles", "s_nbuckets", "s_tile_rows", "s_bucket_len", "g_ntiles", "g_nbuckets",
+              "g_tile_len", "g_bucket_entries_max", "g_bucket_rows_max", "reserved")
+PLAN_TABLES = ("s_tileRows", "s_runStart", "s_src", "s_dst", "g_bucketRows", "g_tileSlot",
+               "g_runStart", "g_src", "g_pos")
+
+
+class PlanDev(ctypes.Structure):
+    _fields_ = ([(k, ctypes.c_int32) for k in _PLAN_INTS]
+                + [(k, ctypes.c_void_p) for k in PLAN_TABLES]
+                + [("work", ctypes.c_void_p), ("work_len", ctypes.c_int64)])
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = ([(k, ctypes.c_int32) for k in (
+        "valid", "s_tile_rows", "s_bucket_len", "g_tile_len", "g_bucket_entries", "s_ntiles",
+        "s_nbuckets", "g_ntiles", "g_nbuckets", "g_bucket_rows_max", "g_bucket_entries_max",
+        "reserved")]
+        + [(k, ctypes.c_int64) for k in ("smem_s1", "smem_s2", "smem_g1", "smem_g2")])
+
+
 class GSDev(ctypes.Structure):
     _fields_ = [("NL", ctypes.c_int64), ("NG", ctypes.c_int64), ("nnz", ctypes.c_int64),
                 ("nblocks", ctypes.c_int64), ("seg_max", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("scatterIds", ctypes.c_void_p),
                 ("rowStarts", ctypes.c_void_p), ("localIds", ctypes.c_void_p),
-                ("blockStarts", ctypes.c_void_p)]
+                ("blockStarts", ctypes.c_void_p), ("plan", ctypes.c_void_p)]
 
 
 _vp = ctypes.c_void_p
@@ -100,6 +120,9 @@ def _declare(lib):
         "bs_cg_iteration": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 10, _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
+        "bs_mesh_plan": ([_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], _int),
+        "bs_mesh_plan_info": ([_vp, ctypes.POINTER(PlanInfo)], _int),
+        "bs_mesh_plan_tables": ([_vp] + [ctypes.POINTER(_vp)] * 9, _int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -331,8 +354,51 @@ class Mesh:
                 out[name] = np.frombuffer(buf, dtype=np.int32).copy()
         return out
 
-    def to_device(self, device=None):
-        return DeviceTables.from_host(self.tables(), self.info, device)
+    def plan(self, s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries):
+        """Rebuild the two-pass plan with other tile/bucket sizes (returns the status)."""
+        return lib.bs_mesh_plan(self.handle, int(s_tile_rows), int(s_bucket_len), int(g_tile_len),
+                                int(g_bucket_entries))
+
+    def plan_info(self):
+        info = PlanInfo()
+        lib.bs_mesh_plan_info(self.handle, ctypes.byref(info))
+        return info
+
+    def plan_tables(self):
+        """Copies of the plan's host tables (int32 / uint16 numpy arrays), or None."""
+        pi = self.plan_info()
+        if not pi.valid:
+            return None
+        ptrs = [_vp() for _ in PLAN_TABLES]
+        st = lib.bs_mesh_plan_tables(self.handle, *[ctypes.byref(p) for p in ptrs])
+        if st != BS_OK:
+            raise BSError(st, "bs_mesh_plan_tables")
+        sizes = {"s_tileRows": (pi.s_ntiles + 1, np.int32),
+                 "s_runStart": ((pi.s_ntiles + 1) * pi.s_nbuckets, np.int32),
+                 "s_src": (self.nnz, np.uint16), "s_dst": (self.nnz, np.uint16),
+                 "g_bucketRows": (pi.g_nbuckets + 1, np.int32),
+                 "g_tileSlot": (pi.g_ntiles + 1, np.int32),
+                 "g_runStart": ((pi.g_ntiles + 1) * pi.g_nbuckets, np.int32),
+                 "g_src": (self.nnz, np.uint16), "g_pos": (self.nnz, np.uint16)}
+        out = {}
+        for name, p in zip(PLAN_TABLES, ptrs):
+            n, dt = sizes[name]
+            if n == 0:
+                out[name] = np.zeros(0, dtype=dt)
+            else:
+                ct = ctypes.c_int32 if dt == np.int32 else ctypes.c_uint16
+                out[name] = np.frombuffer((ct * n).from_address(p.value), dtype=dt).copy()
+        return out
+
+    def to_device(self, device=None, planned=True):
+        """Upload the tables; with planned=True (and a valid plan) also the
+        two-pass plan and its work buffer, so bs_gather/bs_scatter use it."""
+        plan = None
+        if planned:
+            pt = self.plan_tables()
+            if pt is not None:
+                plan = (pt, self.plan_info())
+        return DeviceTables.from_host(self.tables(), self.info, device, plan)
 
 
 class DeviceTables:
@@ -352,16 +418,48 @@ class DeviceTables:
             return t.data_ptr() if t.numel() else 0
 
         self.struct = GSDev(NL, NG, nnz, nblocks, seg_max, 0, ptr(scatterIds), ptr(rowStarts),
-                            ptr(localIds), ptr(blockStarts))
+                            ptr(localIds), ptr(blockStarts), None)
+        self.plan = None
+        self.plan_struct = None
+
+    def attach_plan(self, tabs, pinfo):
+        """Upload a two-pass plan (host tables + PlanInfo) and allocate its work buffer."""
+        dev = self.scatterIds.device
+        up = {}
+        for k in PLAN_TABLES:
+            a = np.ascontiguousarray(tabs[k])
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)        # same bits; torch has no general uint16 kernels
+            up[k] = torch.from_numpy(a).to(dev)
+        work = torch.empty(max(self.nnz, 1), dtype=torch.float64, device=dev)
+        ints = dict(s_ntiles=pinfo.s_ntiles, s_nbuckets=pinfo.s_nbuckets,
+                    s_tile_rows=pinfo.s_tile_rows, s_bucket_len=pinfo.s_bucket_len,
+                    g_ntiles=pinfo.g_ntiles, g_nbuckets=pinfo.g_nbuckets,
+                    g_tile_len=pinfo.g_tile_len, g_bucket_entries_max=pinfo.g_bucket_entries_max,
+                    g_bucket_rows_max=pinfo.g_bucket_rows_max, reserved=0)
+        ps = PlanDev(**ints, **{k: (up[k].data_ptr() if up[k].numel() else 0) for k in PLAN_TABLES},
+                     work=work.data_ptr(), work_len=self.nnz)
+        self.plan = dict(up, work=work, info=pinfo)
+        self.plan_struct = ps
+        self.struct.plan = ctypes.addressof(ps)
+        return self
+
+    def detach_plan(self):
+        self.struct.plan = None
+        self.plan = None
+        self.plan_struct = None
+        return self
 
     @classmethod
-    def from_host(cls, tabs, info, device=None):
+    def from_host(cls, tabs, info, device=None, plan=None):
         dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
         up = {k: torch.from_numpy(np.ascontiguousarray(v, dtype=np.int32)).to(dev)
               for k, v in tabs.items()}
-        return cls(up["scatterIds"], up["rowStarts"], up["localIds"], up["blockStarts"],
-                   int(info.NL), int(info.NG), int(info.nnz), int(info.nblocks),
-                   int(info.seg_max))
+        t = cls(up["scatterIds"], up["rowStarts"], up["localIds"], up["blockStarts"],
+                int(info.NL), int(info.NG), int(info.nnz), int(info.nblocks), int(info.seg_max))
+        if plan is not None:
+            t.attach_plan(*plan)
+        return t
 
     @property
     def device(self):
@@ -369,8 +467,11 @@ class DeviceTables:
 
     @property
     def nbytes(self):
-        return sum(t.numel() * 4 for t in (self.scatterIds, self.rowStarts, self.localIds,
-                                            self.blockStarts))
+        n = sum(t.numel() * 4 for t in (self.scatterIds, self.rowStarts, self.localIds,
+                                         self.blockStarts))
+        if self.plan is not None:
+            n += sum(self.plan[k].numel() * self.plan[k].element_size() for k in PLAN_TABLES)
+        return n
 
 
 # ------------------------------------------------------------ BS6 / BS7

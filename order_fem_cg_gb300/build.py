@@ -1,6 +1,6 @@
 """Builds libbs.so in-tree with nvcc for sm_103a (GB300).
 
-Four translation units are compiled in parallel and linked with the static
+The translation units are compiled in parallel and linked with the static
 CUDA runtime, so the library needs only the driver (libcuda) at run time.
 Run as ``python order_fem_cg_gb300/build.py`` (it does not import the package,
 whose import needs the library built here).
@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libbs.so")
 OBJDIR = os.path.join(ROOT, "_build", "libbs")
 
-SOURCES = ["bs_ctx.cu", "bs_vec.cu", "bs_gs.cu", "bs_mesh.cpp"]
+SOURCES = ["bs_ctx.cu", "bs_vec.cu", "bs_gs.cu", "bs_gs2.cu", "bs_mesh.cpp", "bs_plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -134,9 +134,14 @@ __global__ void __launch_bounds__(kThreads)
         double s = 0.0;
         if (z < a) {
             bad = true;
-        } else {
-            for (int32_t j = a; j < z; ++j)
+        } else if (z > a) {
+            // (+0.0 + v_a) + ... equals v_a + ... except that it is never
+            // -0.0: skip the first addition, then map -0.0 to +0.0.
+            s = vals[a];
+            for (int32_t j = a + 1; j < z; ++j)
                 s += vals[j];
+            if ((__double_as_longlong(s) << 1) == 0)
+                s = 0.0;
         }
         qG[r0 + k] = s;
     }
@@ -269,6 +274,8 @@ extern "C" int bs_gather(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, doub
     if (t->NG == 0)
         return BS_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (t->plan)
+        return bs_gather_planned(ctx, t, qL, qG, s);
     if (t->seg_max <= 1024)
         launch_gather<1024>(ctx, t, qL, qG, s);
     else if (t->seg_max <= 2048)
@@ -297,6 +304,8 @@ extern "C" int bs_scatter(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, dou
     if (t->NL == 0)
         return BS_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (t->plan)
+        return bs_scatter_planned(ctx, t, qG, qL, s);
     const bool vec = (reinterpret_cast<uintptr_t>(t->scatterIds) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(qL) & 31u) == 0;
     const int64_t cap = static_cast<int64_t>(ctx->sms) * ctx->tune.scatter_blocks_per_sm;

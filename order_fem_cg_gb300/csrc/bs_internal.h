@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cstdio>
 
+#include <cuda_runtime.h>
+
 #include "bs.h"
 
 // Reduction workspace capacity: one partial sum per block of a reduction.
@@ -53,6 +55,13 @@ int bs_check_device(bs_ctx *ctx);
             return bs_set_error((ctx), BS_ECUDA, "launch of %s: %s", (what),                     \
                                 cudaGetErrorString(e_));                                         \
     } while (0)
+
+// Two-pass tiled gather/scatter (bs_gs2.cu); t->plan is non-NULL and the
+// common arguments are already validated.
+int bs_scatter_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, double *qL,
+                       cudaStream_t s);
+int bs_gather_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double *qG,
+                      cudaStream_t s);
 
 // Do the byte ranges [a, a+na) and [b, b+nb) overlap?
 inline bool bs_overlap(const void *a, int64_t na, const void *b, int64_t nb)

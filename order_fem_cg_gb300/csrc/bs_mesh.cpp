@@ -21,15 +21,7 @@
 #include <thread>
 #include <vector>
 
-#include "bs.h"
-
-struct bs_mesh {
-    int32_t E = 0, N = 0;
-    uint32_t flags = 0;
-    int32_t max_row = 0, seg_max = 0, seg_target = 0;
-    int64_t K = 0, NL = 0, NG = 0, nnz = 0;
-    std::vector<int32_t> scatterIds, rowStarts, localIds, blockStarts;
-};
+#include "bs_mesh_impl.h"
 
 namespace {
 
@@ -212,6 +204,7 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
         seg_max = std::max<int32_t>(seg_max, static_cast<int32_t>(std::max(ce, cr)));
         m->blockStarts.push_back(static_cast<int32_t>(NG));
         m->seg_max = std::max<int32_t>(seg_max, 1);
+        bs_plan_build(m, BS_TILE_S_ROWS, BS_TILE_S_BUCKET, BS_TILE_G_LOCALS, BS_TILE_G_BUCKET);
     } catch (const std::bad_alloc &) {
         delete m;
         return BS_ENOMEM;
@@ -310,5 +303,66 @@ extern "C" int bs_mesh_validate(const bs_mesh *m)
 extern "C" int bs_mesh_destroy(bs_mesh *m)
 {
     delete m;
+    return BS_OK;
+}
+
+extern "C" int bs_mesh_plan(bs_mesh *m, int32_t s_tile_rows, int32_t s_bucket_len,
+                            int32_t g_tile_len, int32_t g_bucket_entries)
+{
+    if (!m)
+        return BS_EINVAL;
+    try {
+        bs_plan_build(m, s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries);
+    } catch (const std::bad_alloc &) {
+        m->plan = bs_plan();
+        return BS_ENOMEM;
+    }
+    return m->plan.valid ? BS_OK : BS_EINVAL;
+}
+
+extern "C" int bs_mesh_plan_info(const bs_mesh *m, bs_plan_info_t *out)
+{
+    if (!m || !out)
+        return BS_EINVAL;
+    const bs_plan &p = m->plan;
+    std::memset(out, 0, sizeof(*out));
+    out->valid = p.valid ? 1 : 0;
+    out->s_tile_rows = p.s_tile_rows;
+    out->s_bucket_len = p.s_bucket_len;
+    out->g_tile_len = p.g_tile_len;
+    out->g_bucket_entries = p.g_bucket_entries;
+    out->s_ntiles = p.s_ntiles;
+    out->s_nbuckets = p.s_nbuckets;
+    out->g_ntiles = p.g_ntiles;
+    out->g_nbuckets = p.g_nbuckets;
+    out->g_bucket_rows_max = p.g_bucket_rows_max;
+    out->g_bucket_entries_max = p.g_bucket_entries_max;
+    if (p.valid) {
+        out->smem_s1 = bs_plan_smem_s1(p);
+        out->smem_s2 = bs_plan_smem_s2(p);
+        out->smem_g1 = bs_plan_smem_g1(p);
+        out->smem_g2 = bs_plan_smem_g2(p);
+    }
+    return BS_OK;
+}
+
+extern "C" int bs_mesh_plan_tables(const bs_mesh *m, const int32_t **s_tileRows,
+                                   const int32_t **s_runStart, const uint16_t **s_src,
+                                   const uint16_t **s_dst, const int32_t **g_bucketRows,
+                                   const int32_t **g_tileSlot, const int32_t **g_runStart,
+                                   const uint16_t **g_src, const uint16_t **g_pos)
+{
+    if (!m || !m->plan.valid)
+        return BS_EINVAL;
+    const bs_plan &p = m->plan;
+    if (s_tileRows) *s_tileRows = p.s_tileRows.data();
+    if (s_runStart) *s_runStart = p.s_runStart.data();
+    if (s_src) *s_src = p.s_src.data();
+    if (s_dst) *s_dst = p.s_dst.data();
+    if (g_bucketRows) *g_bucketRows = p.g_bucketRows.data();
+    if (g_tileSlot) *g_tileSlot = p.g_tileSlot.data();
+    if (g_runStart) *g_runStart = p.g_runStart.data();
+    if (g_src) *g_src = p.g_src.data();
+    if (g_pos) *g_pos = p.g_pos.data();
     return BS_OK;
 }

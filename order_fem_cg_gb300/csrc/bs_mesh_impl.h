@@ -1,0 +1,64 @@
+// bs_mesh_impl.h -- host representation of a mesh and its index tables.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "bs.h"
+
+// Two-pass gather/scatter plan: the permutation between global (CSR) order
+// and local order done through shared memory in two coalesced passes.
+//
+// Scatter (q_L = Z q_G): pass 1 takes a tile of consecutive global rows,
+// holds their q_G values in shared memory and writes, for every bucket of
+// consecutive locals, one contiguous run of the work array; pass 2 takes one
+// bucket's runs, places them by local offset in shared memory and writes the
+// bucket's q_L range coalesced.  Gather (q_G = Z^T q_L) mirrors it: pass 1
+// tiles consecutive locals, buckets are ranges of consecutive rows; pass 2
+// places a bucket's values by CSR position and sums each row in ascending
+// local order.  The work array is ordered bucket-major, then tile, so both
+// passes touch it in runs.
+struct bs_plan {
+    bool valid = false;
+    int32_t s_tile_rows = 0, s_bucket_len = 0, g_tile_len = 0, g_bucket_entries = 0;
+    int32_t s_ntiles = 0, s_nbuckets = 0, g_ntiles = 0, g_nbuckets = 0;
+    int32_t g_bucket_rows_max = 0, g_bucket_entries_max = 0;
+    std::vector<int32_t> s_tileRows;   // [s_ntiles+1]  first row of each scatter tile
+    std::vector<int32_t> s_runStart;   // [(s_ntiles+1) x s_nbuckets] work position of run (t, b)
+    std::vector<uint16_t> s_src;       // [nnz] tile-major: row offset within the tile
+    std::vector<uint16_t> s_dst;       // [nnz] work order: local offset within the bucket
+    std::vector<int32_t> g_bucketRows; // [g_nbuckets+1] first row of each gather bucket
+    std::vector<int32_t> g_tileSlot;   // [g_ntiles+1]  unmasked locals before each tile
+    std::vector<int32_t> g_runStart;   // [(g_ntiles+1) x g_nbuckets]
+    std::vector<uint16_t> g_src;       // [nnz] tile-major: local offset within the tile
+    std::vector<uint16_t> g_pos;       // [nnz] work order: CSR position within the bucket
+};
+
+struct bs_mesh {
+    int32_t E = 0, N = 0;
+    uint32_t flags = 0;
+    int32_t max_row = 0, seg_max = 0, seg_target = 0;
+    int64_t K = 0, NL = 0, NG = 0, nnz = 0;
+    std::vector<int32_t> scatterIds, rowStarts, localIds, blockStarts;
+    bs_plan plan;
+};
+
+// Default plan sizes: each fills most of a GB300 SM's 227 KB of shared
+// memory (8 bytes per staged value).
+constexpr int32_t BS_TILE_S_ROWS = 24576;
+constexpr int32_t BS_TILE_S_BUCKET = 24576;
+constexpr int32_t BS_TILE_G_LOCALS = 24576;
+constexpr int32_t BS_TILE_G_BUCKET = 22528;
+// Largest dynamic shared memory of one block.
+constexpr int64_t BS_SMEM_MAX = 232448;
+
+// Shared-memory bytes the four plan kernels need.
+int64_t bs_plan_smem_s1(const bs_plan &p);
+int64_t bs_plan_smem_s2(const bs_plan &p);
+int64_t bs_plan_smem_g1(const bs_plan &p);
+int64_t bs_plan_smem_g2(const bs_plan &p);
+
+// (Re)builds m->plan; leaves it invalid (empty) when a kernel would need
+// more shared memory than a block can have.  Throws std::bad_alloc.
+void bs_plan_build(bs_mesh *m, int32_t s_tile_rows, int32_t s_bucket_len, int32_t g_tile_len,
+                   int32_t g_bucket_entries);

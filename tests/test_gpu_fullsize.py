@@ -1,0 +1,71 @@
+"""Parity at full size: the stress mesh (56,623,104 local / 33,076,161 global
+nodes) in exactly the configuration bench.py times, every output of one step
+compared with the oracle on the whole arrays (bit-exact, or 1e-12 relative
+for the reductions)."""
+
+import numpy as np
+import pytest
+
+import bsinputs as gen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+from conftest import build_lib  # noqa: E402
+
+build_lib()
+import bench  # noqa: E402
+import order_fem_cg_gb300 as bs  # noqa: E402
+
+
+def same(a, b):
+    return np.array_equal(np.asarray(a).view(np.uint64), np.asarray(b).view(np.uint64))
+
+
+def close(a, b, rtol=1e-12):
+    return abs(a - b) <= rtol * abs(b)
+
+
+@pytest.mark.parametrize("planned", [True, False])
+def test_stress_step_matches_oracle(planned):
+    cfg = gen.CONFIGS["stress"]
+    torch.cuda.set_device(0)
+    wl = bench.Workload(cfg, torch, bs, torch.device("cuda", 0), planned=planned)
+    assert wl.planned == planned
+    h, v, sc = wl.h, wl.v, wl.sc
+    ep, npm = gen.mesh_perms(cfg)
+    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm)
+    assert np.array_equal(wl.mesh.tables()["scatterIds"], ids)
+    stream = torch.cuda.current_stream()
+    for name in wl.names:
+        wl.op(name, stream)
+    torch.cuda.synchronize()
+
+    def g(k):
+        return v[k].cpu().numpy()
+
+    def s(k):
+        return sc[k].cpu().item()
+
+    assert same(g("b"), h["u"])
+    assert same(g("d"), oracle.axpy(cfg.alpha, h["p"], cfg.beta, h["r"]))
+    assert close(s("norm"), oracle.norm(h["Ap"]))
+    assert close(s("dot"), oracle.dot(h["x"], h["u"]))
+    xo, ro, rro = oracle.cg_update(cfg.alpha, h["p"], h["Ap"], h["x"], h["r"])
+    assert same(g("X"), xo) and same(g("R"), ro) and close(s("rdotr"), rro)
+    del xo, ro
+    assert same(g("qG1"), oracle.gather(ids, h["u"], cfg.NG))
+    assert same(g("qL2"), oracle.scatter(ids, h["qG"]))
+    ref = oracle.cg_sequence(ids, h["pG"], h["xG"], h["rG"], wl.rr_host)
+    assert same(g("pL"), ref["pL"]) and same(g("ApG"), ref["ApG"])
+    assert close(s("pAp"), ref["pAp"])
+    da = 2e-12 * abs(ref["alpha"])
+    xg, rg = g("xG"), g("rG")
+    assert np.all(np.abs(xg - ref["x"]) <= da * np.abs(h["pG"]) + np.spacing(np.abs(ref["x"])))
+    assert np.all(np.abs(rg - ref["r"]) <= da * np.abs(ref["ApG"]) + np.spacing(np.abs(ref["r"])))
+    assert close(s("rnorm"), oracle.norm(rg))
+    assert bs.default_context().device_status() == bs.BS_OK

@@ -155,14 +155,18 @@ def test_reductions_bitwise_reproducible_large():
 
 # ------------------------------------------------------------- meshes
 
-def mesh_case(cfg, seg=None):
+def mesh_case(cfg, seg=None, planned=False, sizes=None):
     m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags, seg_target=seg)
     assert m.validate() == bs.BS_OK
+    if sizes is not None:
+        assert m.plan(*sizes) == bs.BS_OK
     ids = m.tables()["scatterIds"]
     ep, npm = gen.mesh_perms(cfg)
     ids_o = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
     assert np.array_equal(ids, ids_o)
-    return m, m.to_device(0), ids_o
+    t = m.to_device(0, planned=planned)
+    assert (t.plan is not None) == planned
+    return m, t, ids_o
 
 
 MESHES = [
@@ -178,9 +182,29 @@ MESHES = [
 ]
 
 
+PLANNED = [
+    (gen.CONFIGS["tiny"], None),
+    (gen.CONFIGS["tiny"], (100, 64, 200, 150)),
+    (gen.CONFIGS["tiny"], (7, 5, 9, 8)),
+    (gen.MeshConfig("masked", 6, 4, 17, 7), (500, 333, 700, 600)),
+    (gen.MeshConfig("one", 1, 1, 5, 3), None),
+    (gen.MeshConfig("onemask", 1, 3, 5, 7), (3, 5, 7, 9)),
+    (gen.CONFIGS["mid"], None),
+    (gen.CONFIGS["large"], None),
+]
+
+
 @pytest.mark.parametrize("cfg,seg", MESHES, ids=lambda v: getattr(v, "name", str(v)))
 def test_scatter_gather(cfg, seg):
-    m, t, ids = mesh_case(cfg, seg)
+    check_scatter_gather(cfg, *mesh_case(cfg, seg))
+
+
+@pytest.mark.parametrize("cfg,sizes", PLANNED, ids=lambda v: getattr(v, "name", str(v)))
+def test_scatter_gather_two_pass(cfg, sizes):
+    check_scatter_gather(cfg, *mesh_case(cfg, planned=True, sizes=sizes))
+
+
+def check_scatter_gather(cfg, m, t, ids):
     qG = gen.uniform_pm1(cfg.seed, gen.TAG_U, cfg.NG)
     qL = gen.uniform_pm1(cfg.seed, gen.TAG_P, cfg.NL)
     qLd = dev(np.zeros(cfg.NL))
@@ -192,19 +216,25 @@ def test_scatter_gather(cfg, seg):
     assert bs.default_context().device_status() == bs.BS_OK
 
 
-def test_scatter_unaligned_views():
+@pytest.mark.parametrize("planned", [False, True])
+def test_scatter_gather_unaligned_views(planned):
     cfg = gen.CONFIGS["tiny"]
-    m, t, ids = mesh_case(cfg)
+    m, t, ids = mesh_case(cfg, planned=planned)
     qG = gen.uniform_pm1(1, 1, cfg.NG)
-    qLd = dev(np.zeros(cfg.NL), 1)            # 8-byte aligned only: scalar path
+    qLd = dev(np.zeros(cfg.NL), 1)            # 8-byte aligned only
     bs.bs_scatter(t, dev(qG, 3), qLd)
     assert bits_equal(host(qLd), oracle.scatter(ids, qG))
+    qL = gen.uniform_pm1(1, 2, cfg.NL)
+    qGd = dev(np.zeros(cfg.NG), 1)
+    bs.bs_gather(t, dev(qL, 3), qGd)
+    assert bits_equal(host(qGd), oracle.gather(ids, qL, cfg.NG))
 
 
-def test_gather_sum_order_probe():
+@pytest.mark.parametrize("planned", [False, True])
+def test_gather_sum_order_probe(planned):
     """Rows whose sum depends on order: 1.0 at the smallest local id, 2^-53 elsewhere."""
     cfg = gen.CONFIGS["tiny"]
-    m, t, ids = mesh_case(cfg)
+    m, t, ids = mesh_case(cfg, planned=planned, sizes=(50, 40, 60, 64) if planned else None)
     tabs = m.tables()
     rs, li = tabs["rowStarts"], tabs["localIds"]
     for first in (True, False):
@@ -216,9 +246,10 @@ def test_gather_sum_order_probe():
         assert bits_equal(host(qGd), oracle.gather(ids, qL, cfg.NG))
 
 
-def test_gather_of_ones_and_identities():
+@pytest.mark.parametrize("planned", [False, True])
+def test_gather_of_ones_and_identities(planned):
     cfg = gen.CONFIGS["mid"]
-    m, t, ids = mesh_case(cfg)
+    m, t, ids = mesh_case(cfg, planned=planned)
     mult = dev(np.zeros(cfg.NG))
     bs.bs_gather(t, dev(np.ones(cfg.NL)), mult)
     mh = host(mult)
@@ -261,6 +292,24 @@ def test_out_of_range_entry_is_flagged_not_dereferenced():
     assert ctx.device_status() == bs.BS_OK   # the flag was cleared by the read
 
 
+def test_bad_plan_entry_is_flagged_not_dereferenced():
+    cfg = gen.CONFIGS["tiny"]
+    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    assert m.plan(100, 64, 200, 150) == bs.BS_OK
+    pt, pi = m.plan_tables(), m.plan_info()
+    for key, bad in (("s_dst", 65535), ("s_src", 65535), ("g_src", 65535), ("g_pos", 65535)):
+        corrupt = dict(pt)
+        corrupt[key] = pt[key].copy()
+        corrupt[key][17] = bad
+        t = bs.DeviceTables.from_host(m.tables(), m.info, 0, (corrupt, pi))
+        ctx = bs.default_context()
+        assert ctx.device_status() == bs.BS_OK
+        qLd, qGd = dev(np.zeros(cfg.NL)), dev(np.zeros(cfg.NG))
+        bs.bs_scatter(t, dev(gen.uniform_pm1(1, 1, cfg.NG)), qLd)
+        bs.bs_gather(t, dev(gen.uniform_pm1(1, 2, cfg.NL)), qGd)
+        assert ctx.device_status() == bs.BS_EBOUNDS, key
+
+
 def test_invalid_arguments_rejected():
     x = dev(np.zeros(10))
     with pytest.raises(ValueError):
@@ -279,10 +328,11 @@ def test_invalid_arguments_rejected():
 
 # ---------------------------------------------------------- CG sequence
 
-@pytest.mark.parametrize("name", ["tiny", "mid"])
-def test_cg_iteration_sequence(name):
+@pytest.mark.parametrize("name,planned", [("tiny", False), ("mid", False), ("tiny", True),
+                                          ("mid", True)])
+def test_cg_iteration_sequence(name, planned):
     cfg = gen.CONFIGS[name]
-    m, t, ids = mesh_case(cfg)
+    m, t, ids = mesh_case(cfg, planned=planned)
     NG = cfg.NG
     pG = gen.uniform_pm1(cfg.seed, gen.TAG_P, NG)
     xG = gen.uniform_pm1(cfg.seed, gen.TAG_X, NG)

@@ -121,3 +121,90 @@ def test_seeded_permutation_matches_generator(bs):
     ex, ey, ez = e % 7, (e // 7) % 7, e // 49
     M = 8
     assert np.array_equal(ids[:, 0], npm[ex + M * (ey + M * ez)])
+
+
+# ------------------------------------------------- two-pass plan (host)
+
+def _seq_row_sums(vals, starts, lens):
+    """Row sums from +0.0 in ascending order (vectorised over rows)."""
+    s = np.zeros(len(starts))
+    for k in range(int(lens.max()) if len(lens) else 0):
+        m = lens > k
+        s[m] = s[m] + vals[starts[m] + k]
+    return s
+
+
+def simulate_plan_scatter(pt, pi, tabs, qG, NL):
+    T, B, BL = pi.s_ntiles, pi.s_nbuckets, pi.s_bucket_len
+    rs, tr = tabs["rowStarts"], pt["s_tileRows"]
+    run = pt["s_runStart"].reshape(T + 1, B)
+    work = np.full(len(pt["s_src"]), np.nan)
+    for t in range(T):
+        r0, r1 = tr[t], tr[t + 1]
+        off = np.concatenate([[0], np.cumsum(run[t + 1] - run[t])])
+        assert off[-1] == rs[r1] - rs[r0]
+        k = np.arange(off[-1])
+        c = np.searchsorted(off, k, side="right") - 1
+        work[run[t][c] + (k - off[c])] = qG[r0:r1][pt["s_src"][rs[r0] + k]]
+    qL = np.zeros(NL)
+    for b in range(B):
+        j0, j1 = run[0, b], run[T, b]
+        qL[b * BL + pt["s_dst"][j0:j1].astype(np.int64)] = work[j0:j1]
+    return qL
+
+
+def simulate_plan_gather(pt, pi, tabs, qL, NG):
+    U, C, TL = pi.g_ntiles, pi.g_nbuckets, pi.g_tile_len
+    rs, br, ts = tabs["rowStarts"], pt["g_bucketRows"], pt["g_tileSlot"]
+    run = pt["g_runStart"].reshape(U + 1, C)
+    work = np.full(len(pt["g_src"]), np.nan)
+    for u in range(U):
+        off = np.concatenate([[0], np.cumsum(run[u + 1] - run[u])])
+        assert off[-1] == ts[u + 1] - ts[u]
+        k = np.arange(off[-1])
+        c = np.searchsorted(off, k, side="right") - 1
+        work[run[u][c] + (k - off[c])] = qL[u * TL:(u + 1) * TL][pt["g_src"][ts[u] + k]]
+    qG = np.zeros(NG)
+    for c in range(C):
+        r0, r1 = br[c], br[c + 1]
+        e0, e1 = rs[r0], rs[r1]
+        assert run[0, c] == e0 and run[U, c] == e1
+        vals = np.empty(e1 - e0)
+        vals[pt["g_pos"][e0:e1].astype(np.int64)] = work[e0:e1]
+        qG[r0:r1] = _seq_row_sums(vals, rs[r0:r1] - e0, np.diff(rs[r0:r1 + 1]))
+    return qG
+
+
+PLAN_CASES = [("tiny", None), ("tiny", (100, 64, 200, 150)), ("tiny", (7, 5, 9, 8)),
+              ("mid", None), ((5, 3, 7), (300, 256, 500, 333)), ((3, 4, 3), None)]
+
+
+@pytest.mark.parametrize("which,sizes", PLAN_CASES)
+def test_two_pass_plan_reproduces_oracle(bs, which, sizes):
+    if isinstance(which, str):
+        cfg = gen.CONFIGS[which]
+    else:
+        E, N, flags = which
+        cfg = gen.MeshConfig("t", E, N, 0x51 + E, flags)
+    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    if sizes is not None:
+        assert m.plan(*sizes) == bs.BS_OK
+    pi = m.plan_info()
+    assert pi.valid
+    assert max(pi.smem_s1, pi.smem_s2, pi.smem_g1, pi.smem_g2) <= 232448
+    pt, tabs = m.plan_tables(), m.tables()
+    ids = tabs["scatterIds"]
+    qG = gen.uniform_pm1(cfg.seed, gen.TAG_U, cfg.NG)
+    qL = gen.uniform_pm1(cfg.seed, gen.TAG_P, cfg.NL)
+    got_s = simulate_plan_scatter(pt, pi, tabs, qG, cfg.NL)
+    assert np.array_equal(got_s.view(np.uint64), oracle.scatter(ids, qG).view(np.uint64))
+    got_g = simulate_plan_gather(pt, pi, tabs, qL, cfg.NG)
+    assert np.array_equal(got_g.view(np.uint64), oracle.gather(ids, qL, cfg.NG).view(np.uint64))
+
+
+def test_plan_rejects_bad_sizes_and_oversized_smem(bs):
+    m = bs.Mesh(4, 3, 1)
+    assert m.plan(0, 10, 10, 10) == bs.BS_EINVAL and not m.plan_info().valid
+    assert m.plan(10, 70000, 10, 10) == bs.BS_EINVAL
+    assert m.plan(30000, 30000, 30000, 30000) == bs.BS_EINVAL    # > 227 KB of shared memory
+    assert m.plan(24576, 24576, 24576, 22528) == bs.BS_OK and m.plan_info().valid
