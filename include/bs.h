@@ -96,20 +96,24 @@ typedef struct {
  * All table pointers are device memory uploaded by the caller from
  * bs_mesh_plan_tables(); `work` is caller-owned device scratch of at least
  * nnz binary64 values, overwritten by every bs_gather / bs_scatter call
- * that uses the plan (so two such calls must not overlap on the GPU). */
+ * that uses the plan (so two such calls must not overlap on the GPU).
+ * Sizes are per thread block; a tile or bucket is `cluster` blocks. */
 typedef struct {
+    int32_t cluster;
     int32_t s_ntiles, s_nbuckets, s_tile_rows, s_bucket_len;
     int32_t g_ntiles, g_nbuckets, g_tile_len, g_bucket_entries_max;
-    int32_t g_bucket_rows_max, reserved;
+    int32_t g_bucket_rows_max, g_mmax;
     const int32_t *s_tileRows;   /* [s_ntiles+1]                    */
     const int32_t *s_runStart;   /* [(s_ntiles+1) * s_nbuckets]     */
     const uint16_t *s_src;       /* [nnz]                           */
     const uint16_t *s_dst;       /* [nnz]                           */
-    const int32_t *g_bucketRows; /* [g_nbuckets+1]                  */
+    const int32_t *g_subRows;    /* [cluster * g_nbuckets + 1]      */
     const int32_t *g_tileSlot;   /* [g_ntiles+1]                    */
     const int32_t *g_runStart;   /* [(g_ntiles+1) * g_nbuckets]     */
     const uint16_t *g_src;       /* [nnz]                           */
     const uint16_t *g_pos;       /* [nnz]                           */
+    const uint16_t *g_groupStart; /* [cluster*g_nbuckets*(g_mmax+1)] */
+    const uint16_t *g_rowPos;    /* [NG]                            */
     double *work;                /* [work_len >= nnz] scratch       */
     int64_t work_len;
 } bs_plan_dev;
@@ -214,38 +218,44 @@ int bs_mesh_validate(const bs_mesh *mesh);
 int bs_mesh_destroy(bs_mesh *mesh);
 
 /* Two-pass gather/scatter plan, built with every mesh (default sizes) and
- * rebuilt by bs_mesh_plan with other sizes.  It reorders the same sums: the
- * results are bitwise those of the one-pass kernels.
- *   Scatter: tiles of s_tile_rows consecutive global rows (their q_G values
- *   staged in shared memory) write, per bucket of s_bucket_len consecutive
- *   locals, one contiguous run of the work array (pass 1); each bucket then
- *   places its runs by local offset in shared memory and writes its q_L
- *   range coalesced (pass 2).
- *   Gather: tiles of g_tile_len consecutive locals write per-bucket runs,
- *   buckets being consecutive rows with at most g_bucket_entries entries
- *   (pass 1); each bucket places its values by CSR position in shared
- *   memory and sums every row in ascending local order (pass 2).
- * Sizes must be 1..65536 (entries <= 65535, >= 8); a plan whose kernels
- * would need more than 227 KB of shared memory is left invalid (valid = 0)
- * and the one-pass kernels must be used. */
+ * rebuilt by bs_mesh_plan with other sizes.  It reorders the data movement
+ * only: the results are bitwise those of the one-pass kernels.
+ *   Scatter: tiles of consecutive global rows (their q_G values staged in
+ *   shared memory) write, per bucket of consecutive locals, one contiguous
+ *   run of the work array (pass 1); each bucket then places its runs by
+ *   local offset in shared memory and writes its q_L range coalesced
+ *   (pass 2).
+ *   Gather: tiles of consecutive locals write per-bucket runs, a bucket
+ *   being `cluster` consecutive sub-buckets of rows with at most
+ *   g_bucket_entries entries and rows each (pass 1); each bucket places its
+ *   values in shared memory grouped by row length, sums every row in
+ *   ascending local order and writes its rows of q_G in order (pass 2).
+ *   Rows may have at most 32 entries (box meshes: 8).
+ * A tile or bucket is held by a cluster of `cluster` (1, 2 or 4) thread
+ * blocks sharing their shared memory; the sizes are per block: a scatter
+ * tile has cluster * s_tile_rows rows, and so on.  cluster * size must be
+ * <= 65536 (entries: <= 65535, g_bucket_entries >= 8).  A plan whose
+ * kernels would need more than 227 KB of shared memory per block is left
+ * invalid (valid = 0); then use the one-pass kernels. */
 typedef struct {
-    int32_t valid;
+    int32_t valid, cluster;
     int32_t s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries;
     int32_t s_ntiles, s_nbuckets, g_ntiles, g_nbuckets;
     int32_t g_bucket_rows_max, g_bucket_entries_max;
-    int32_t reserved;
+    int32_t g_mmax, reserved;                   /* longest row (<= 32) */
     int64_t smem_s1, smem_s2, smem_g1, smem_g2; /* bytes per block */
 } bs_plan_info_t;
 int bs_mesh_plan(bs_mesh *mesh, int32_t s_tile_rows, int32_t s_bucket_len, int32_t g_tile_len,
-                 int32_t g_bucket_entries);
+                 int32_t g_bucket_entries, int32_t cluster);
 int bs_mesh_plan_info(const bs_mesh *mesh, bs_plan_info_t *out);
 /* Host views of the plan's tables (owned by the mesh); any output may be
  * NULL.  BS_EINVAL if the plan is invalid. */
 int bs_mesh_plan_tables(const bs_mesh *mesh, const int32_t **s_tileRows,
                         const int32_t **s_runStart, const uint16_t **s_src, const uint16_t **s_dst,
-                        const int32_t **g_bucketRows, const int32_t **g_tileSlot,
+                        const int32_t **g_subRows, const int32_t **g_tileSlot,
                         const int32_t **g_runStart, const uint16_t **g_src,
-                        const uint16_t **g_pos);
+                        const uint16_t **g_pos, const uint16_t **g_groupStart,
+                        const uint16_t **g_rowPos);
 
 /* ---- BS6 / BS7 -----------------------------------------------------------
  * "Portable high-order finite element kernels I": the BS6 gather kernel

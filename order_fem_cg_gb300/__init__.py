@@ -60,10 +60,10 @@ class MeshInfo(ctypes.Structure):
                 ("seg_max", ctypes.c_int32), ("seg_target", ctypes.c_int32)]
 
 
-_PLAN_INTS = ("s_ntiles", "s_nbuckets", "s_tile_rows", "s_bucket_len", "g_ntiles", "g_nbuckets",
-              "g_tile_len", "g_bucket_entries_max", "g_bucket_rows_max", "reserved")
-PLAN_TABLES = ("s_tileRows", "s_runStart", "s_src", "s_dst", "g_bucketRows", "g_tileSlot",
-               "g_runStart", "g_src", "g_pos")
+_PLAN_INTS = ("cluster", "s_ntiles", "s_nbuckets", "s_tile_rows", "s_bucket_len", "g_ntiles",
+              "g_nbuckets", "g_tile_len", "g_bucket_entries_max", "g_bucket_rows_max", "g_mmax")
+PLAN_TABLES = ("s_tileRows", "s_runStart", "s_src", "s_dst", "g_subRows", "g_tileSlot",
+               "g_runStart", "g_src", "g_pos", "g_groupStart", "g_rowPos")
 
 
 class PlanDev(ctypes.Structure):
@@ -74,9 +74,9 @@ class PlanDev(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = ([(k, ctypes.c_int32) for k in (
-        "valid", "s_tile_rows", "s_bucket_len", "g_tile_len", "g_bucket_entries", "s_ntiles",
-        "s_nbuckets", "g_ntiles", "g_nbuckets", "g_bucket_rows_max", "g_bucket_entries_max",
-        "reserved")]
+        "valid", "cluster", "s_tile_rows", "s_bucket_len", "g_tile_len", "g_bucket_entries",
+        "s_ntiles", "s_nbuckets", "g_ntiles", "g_nbuckets", "g_bucket_rows_max",
+        "g_bucket_entries_max", "g_mmax", "reserved")]
         + [(k, ctypes.c_int64) for k in ("smem_s1", "smem_s2", "smem_g1", "smem_g2")])
 
 
@@ -120,9 +120,9 @@ def _declare(lib):
         "bs_cg_iteration": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 10, _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
-        "bs_mesh_plan": ([_vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], _int),
+        "bs_mesh_plan": ([_vp] + [ctypes.c_int32] * 5, _int),
         "bs_mesh_plan_info": ([_vp, ctypes.POINTER(PlanInfo)], _int),
-        "bs_mesh_plan_tables": ([_vp] + [ctypes.POINTER(_vp)] * 9, _int),
+        "bs_mesh_plan_tables": ([_vp] + [ctypes.POINTER(_vp)] * 11, _int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -354,10 +354,10 @@ class Mesh:
                 out[name] = np.frombuffer(buf, dtype=np.int32).copy()
         return out
 
-    def plan(self, s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries):
-        """Rebuild the two-pass plan with other tile/bucket sizes (returns the status)."""
+    def plan(self, s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries, cluster=2):
+        """Rebuild the two-pass plan with other per-block sizes / cluster size (returns the status)."""
         return lib.bs_mesh_plan(self.handle, int(s_tile_rows), int(s_bucket_len), int(g_tile_len),
-                                int(g_bucket_entries))
+                                int(g_bucket_entries), int(cluster))
 
     def plan_info(self):
         info = PlanInfo()
@@ -376,10 +376,12 @@ class Mesh:
         sizes = {"s_tileRows": (pi.s_ntiles + 1, np.int32),
                  "s_runStart": ((pi.s_ntiles + 1) * pi.s_nbuckets, np.int32),
                  "s_src": (self.nnz, np.uint16), "s_dst": (self.nnz, np.uint16),
-                 "g_bucketRows": (pi.g_nbuckets + 1, np.int32),
+                 "g_subRows": (pi.cluster * pi.g_nbuckets + 1, np.int32),
                  "g_tileSlot": (pi.g_ntiles + 1, np.int32),
                  "g_runStart": ((pi.g_ntiles + 1) * pi.g_nbuckets, np.int32),
-                 "g_src": (self.nnz, np.uint16), "g_pos": (self.nnz, np.uint16)}
+                 "g_src": (self.nnz, np.uint16), "g_pos": (self.nnz, np.uint16),
+                 "g_groupStart": (pi.cluster * pi.g_nbuckets * (pi.g_mmax + 1), np.uint16),
+                 "g_rowPos": (self.NG, np.uint16)}
         out = {}
         for name, p in zip(PLAN_TABLES, ptrs):
             n, dt = sizes[name]
@@ -432,11 +434,11 @@ class DeviceTables:
                 a = a.view(np.int16)        # same bits; torch has no general uint16 kernels
             up[k] = torch.from_numpy(a).to(dev)
         work = torch.empty(max(self.nnz, 1), dtype=torch.float64, device=dev)
-        ints = dict(s_ntiles=pinfo.s_ntiles, s_nbuckets=pinfo.s_nbuckets,
+        ints = dict(cluster=pinfo.cluster, s_ntiles=pinfo.s_ntiles, s_nbuckets=pinfo.s_nbuckets,
                     s_tile_rows=pinfo.s_tile_rows, s_bucket_len=pinfo.s_bucket_len,
                     g_ntiles=pinfo.g_ntiles, g_nbuckets=pinfo.g_nbuckets,
                     g_tile_len=pinfo.g_tile_len, g_bucket_entries_max=pinfo.g_bucket_entries_max,
-                    g_bucket_rows_max=pinfo.g_bucket_rows_max, reserved=0)
+                    g_bucket_rows_max=pinfo.g_bucket_rows_max, g_mmax=pinfo.g_mmax)
         ps = PlanDev(**ints, **{k: (up[k].data_ptr() if up[k].numel() else 0) for k in PLAN_TABLES},
                      work=work.data_ptr(), work_len=self.nnz)
         self.plan = dict(up, work=work, info=pinfo)

@@ -24,24 +24,28 @@
 // One 1024-thread block per SM, up to 227 KB of dynamic shared memory.
 // Every table-derived index is checked; a bad one is skipped and raises the
 // context's device error flag.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "bs_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
 constexpr int kT = 1024;  // threads per block
 constexpr int kU = 8;     // independent loads per thread per step
+constexpr int kMaxRow = 32;  // longest row of the grouped gather layout
 
 struct PlanArgs {
     int64_t NL, NG, nnz;
     int32_t s_ntiles, s_nbuckets, s_tile_rows, s_bucket_len;
-    int32_t g_ntiles, g_nbuckets, g_tile_len, g_bucket_entries_max, g_bucket_rows_max;
+    int32_t g_ntiles, g_nbuckets, g_tile_len, g_bucket_entries_max, g_bucket_rows_max, g_mmax;
     const int32_t *rowStarts;
     const int32_t *s_tileRows, *s_runStart;
     const uint16_t *s_src, *s_dst;
-    const int32_t *g_bucketRows, *g_tileSlot, *g_runStart;
-    const uint16_t *g_src, *g_pos;
+    const int32_t *g_subRows, *g_tileSlot, *g_runStart;
+    const uint16_t *g_src, *g_pos, *g_groupStart, *g_rowPos;
     double *work;
     int *err;
 };
@@ -63,6 +67,79 @@ __device__ __forceinline__ double ld_seq(const double *p)
 __device__ __forceinline__ void flag(int *err)
 {
     atomicOr(err, BS_DEVERR_BOUNDS);
+}
+
+// ------------------------------------------- bulk async copies (TMA engine)
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Arms the barrier for `bytes` and copies [src, src + bytes) into shared
+// memory at dst; 16-byte aligned addresses, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Waits for phase 0 of the barrier; gives up after a bounded number of
+// polls (each poll may suspend the thread briefly) and reports false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar)
+{
+    constexpr uint32_t kMaxPolls = 1u << 24;
+    for (uint32_t i = 0; i < kMaxPolls; ++i) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(smem_u32(bar))
+                     : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+
+// Writes [src, src + bytes) of shared memory to global memory by the
+// bulk-copy engine and waits only until the engine has read the source.
+// The caller has made the shared-memory writes visible to the async proxy.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Stages n consecutive doubles into shared memory: by the bulk-copy engine
+// when the source is 16-byte aligned (an odd last element by a thread),
+// else by the threads.  `bar` must be initialised; every thread calls it
+// and later calls stage_wait with the returned flag.
+__device__ __forceinline__ bool stage_start(double *dst, const double *src, int n, uint64_t *bar)
+{
+    const bool bulk = n >= 2 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+    if (bulk) {
+        if (threadIdx.x == 0)
+            bulk_load(dst, src, static_cast<uint32_t>(n & ~1) * 8u, bar);
+        if ((n & 1) && threadIdx.x == 1)
+            dst[n - 1] = src[n - 1];
+    }
+    return bulk;
 }
 
 // Copies n consecutive doubles from global memory into shared memory, kU
@@ -153,18 +230,48 @@ __device__ __forceinline__ int find_run(const int32_t *off, int n, int32_t k)
     return lo;
 }
 
-// Loads the (tile, bucket) run table row of tile `t` into shared memory:
-// runPos[b] = work position of run (t, b), runOff = exclusive scan of the
-// run lengths (runOff[nb] = total).  Returns false (uniformly) on a bad
-// table; the caller flags and leaves.
-__device__ bool load_runs(const int32_t *runStart, int t, int nb, int64_t nnz, int32_t *runPos,
-                          int32_t *runOff)
+// The (tile, bucket) run table row of tile `t`, fetched into registers
+// (issued before the tile staging so both are in flight together), then
+// committed to shared memory: runPos[b] = work position of run (t, b),
+// runOff = exclusive scan of the run lengths (runOff[nb] = total).
+constexpr int kRunRegs = 4;  // run-table entries per thread held in registers
+
+struct RunFetch {
+    int32_t p0[kRunRegs], p1[kRunRegs];
+};
+
+__device__ __forceinline__ RunFetch fetch_runs(const int32_t *runStart, int t, int nb)
+{
+    RunFetch f;
+#pragma unroll
+    for (int j = 0; j < kRunRegs; ++j) {
+        const int b = threadIdx.x + j * kT;
+        f.p0[j] = b < nb ? runStart[static_cast<int64_t>(t) * nb + b] : 0;
+        f.p1[j] = b < nb ? runStart[static_cast<int64_t>(t + 1) * nb + b] : 0;
+    }
+    return f;
+}
+
+// Returns false (uniformly) on a bad table.
+__device__ bool commit_runs(const RunFetch &f, const int32_t *runStart, int t, int nb,
+                            int64_t nnz, int32_t *runPos, int32_t *runOff)
 {
     __shared__ int bad_runs;
     if (threadIdx.x == 0)
         bad_runs = 0;
     __syncthreads();
-    for (int b = threadIdx.x; b < nb; b += kT) {
+#pragma unroll
+    for (int j = 0; j < kRunRegs; ++j) {
+        const int b = threadIdx.x + j * kT;
+        if (b < nb) {
+            const bool ok = f.p0[j] >= 0 && f.p1[j] >= f.p0[j] && f.p1[j] <= nnz;
+            runPos[b] = ok ? f.p0[j] : 0;
+            runOff[b] = ok ? f.p1[j] - f.p0[j] : 0;
+            if (!ok)
+                bad_runs = 1;
+        }
+    }
+    for (int b = threadIdx.x + kRunRegs * kT; b < nb; b += kT) {
         const int32_t p0 = runStart[static_cast<int64_t>(t) * nb + b];
         const int32_t p1 = runStart[static_cast<int64_t>(t + 1) * nb + b];
         const bool ok = p0 >= 0 && p1 >= p0 && p1 <= nnz;
@@ -178,38 +285,56 @@ __device__ bool load_runs(const int32_t *runStart, int t, int nb, int64_t nnz, i
     return bad_runs == 0;
 }
 
-// Writes the tile's slots [0, total) to the work array run by run: slot k
-// of run c goes to work[runPos[c] + k - runOff[c]], its value taken from
-// the staged tile at offset src[base + k].  Each warp takes chunks of
-// 32 kU consecutive slots (lane i: slots i, i+32, ...), so the src loads
-// and the work stores of a warp instruction are contiguous; a lane finds
-// its run by one binary search per chunk and then walks forward.
+// all[i] without a dynamically indexed array (keeps the pointers in
+// registers instead of the local-memory stack).
+template <int CS>
+__device__ __forceinline__ double *pick(double *const *all, int i)
+{
+    if constexpr (CS == 1)
+        return all[0];
+    else if constexpr (CS == 2)
+        return i ? all[1] : all[0];
+    else
+        return i < 2 ? (i ? all[1] : all[0]) : (i == 3 ? all[3] : all[2]);
+}
+
+// Writes the tile's slots [kbeg, kend) to the work array run by run: slot
+// k of run c goes to work[runPos[c] + k - runOff[c]], its value taken from
+// the cluster's staged tile at offset src[base + k] (block o / per holds
+// offsets [o*per, (o+1)*per)).  Each warp takes chunks of 32 kU consecutive
+// slots (lane i: slots i, i+32, ...), so the src loads and the work stores
+// of a warp instruction are contiguous; a lane finds its run by one binary
+// search per chunk and then walks forward.
+template <int CS>
 __device__ __forceinline__ bool emit_runs(const int32_t *runPos, const int32_t *runOff, int nb,
-                                          int32_t total, const uint16_t *src, int64_t base,
-                                          const double *vals, int nvals, double *work)
+                                          int32_t kbeg, int32_t kend, const uint16_t *src,
+                                          int64_t base, double *const *tile, int per, int nvals,
+                                          double *work)
 {
     constexpr int kChunk = 32 * kU;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     bool bad = false;
-    for (int32_t c0 = warp * kChunk; c0 < total; c0 += (kT / 32) * kChunk) {
+    for (int32_t c0 = kbeg + warp * kChunk; c0 < kend; c0 += (kT / 32) * kChunk) {
         uint16_t o[kU];
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int32_t k = c0 + lane + 32 * u;
-            o[u] = k < total ? ld_u16(src + base + k) : 0;
+            o[u] = k < kend ? ld_u16(src + base + k) : 0;
         }
-        int c = find_run(runOff, nb, c0 + lane < total ? c0 + lane : total - 1);
+        int c = find_run(runOff, nb, c0 + lane < kend ? c0 + lane : kend - 1);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const int32_t k = c0 + lane + 32 * u;
-            if (k < total) {
+            if (k < kend) {
                 while (c + 1 < nb && runOff[c + 1] <= k)
                     ++c;
                 double v = 0.0;
-                if (o[u] < nvals)
-                    v = vals[o[u]];
-                else
+                if (o[u] < nvals) {
+                    const int owner = CS == 1 ? 0 : o[u] / per;
+                    v = pick<CS>(tile, owner)[o[u] - owner * per];
+                } else {
                     bad = true;
+                }
                 work[runPos[c] + (k - runOff[c])] = v;
             }
         }
@@ -217,188 +342,367 @@ __device__ __forceinline__ bool emit_runs(const int32_t *runPos, const int32_t *
     return bad;
 }
 
+template <int CS>
+__device__ __forceinline__ void cluster_barrier()
+{
+    if constexpr (CS > 1)
+        cg::this_cluster().sync();
+    else
+        __syncthreads();
+}
+
+template <int CS>
+__device__ __forceinline__ int cluster_rank()
+{
+    if constexpr (CS > 1)
+        return static_cast<int>(cg::this_cluster().block_rank());
+    else
+        return 0;
+}
+
+// Pointers to the same shared-memory array in every block of the cluster.
+template <int CS>
+__device__ __forceinline__ void map_cluster(double *mine, double **all)
+{
+    if constexpr (CS > 1) {
+        cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+        for (int j = 0; j < CS; ++j)
+            all[j] = cl.map_shared_rank(mine, j);
+    } else {
+        all[0] = mine;
+    }
+}
+
 // --------------------------------------------------------------- scatter
+// One cluster per tile of CS * s_tile_rows global rows; block r stages rows
+// [r * s_tile_rows, (r+1) * s_tile_rows) of it and emits 1/CS of the slots.
+template <int CS>
 __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const double *__restrict__ qG)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
     int32_t *runPos = reinterpret_cast<int32_t *>(vals + a.s_tile_rows);
     int32_t *runOff = runPos + a.s_nbuckets;
-    const int t = blockIdx.x;
+    const int r = cluster_rank<CS>();
+    const int t = blockIdx.x / CS;
     const int32_t r0 = a.s_tileRows[t], r1 = a.s_tileRows[t + 1];
     const int32_t nrows = r1 - r0;
-    if (r0 < 0 || nrows < 0 || nrows > a.s_tile_rows || r1 > a.NG) {
-        if (threadIdx.x == 0)
-            flag(a.err);
-        return;
+    bool ok = r0 >= 0 && nrows >= 0 && nrows <= CS * a.s_tile_rows && r1 <= a.NG;
+    const int32_t e0 = ok ? a.rowStarts[r0] : 0, e1 = ok ? a.rowStarts[r1] : 0;
+    ok = ok && e0 >= 0 && e1 >= e0 && e1 <= a.nnz;
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0)
+        mbar_init(&bar);
+    __syncthreads();
+    const int32_t m0 = ok ? min(r * a.s_tile_rows, nrows) : 0;
+    const int32_t m1 = ok ? min((r + 1) * a.s_tile_rows, nrows) : 0;
+    const bool bulk = stage_start(vals, qG + r0 + m0, m1 - m0, &bar);
+    const RunFetch rf = fetch_runs(a.s_runStart, t, a.s_nbuckets);
+    if (!bulk)
+        stage(vals, qG + r0 + m0, m1 - m0);
+    ok = commit_runs(rf, a.s_runStart, t, a.s_nbuckets, a.nnz, runPos, runOff) && ok &&
+         runOff[a.s_nbuckets] == e1 - e0;
+    if (bulk && !mbar_wait(&bar)) {
+        ok = false;
+        mbar_wait(&bar);
     }
-    const int32_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
-    if (e0 < 0 || e1 < e0 || e1 > a.nnz) {
-        if (threadIdx.x == 0)
+    double *tile[CS];
+    map_cluster<CS>(vals, tile);
+    cluster_barrier<CS>();  // every block's slice is staged
+    if (ok) {
+        const int32_t total = e1 - e0;
+        const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
+        const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
+        if (emit_runs<CS>(runPos, runOff, a.s_nbuckets, kb, ke, a.s_src, e0, tile, a.s_tile_rows,
+                          nrows, a.work))
             flag(a.err);
-        return;
-    }
-    stage(vals, qG + r0, nrows);
-    if (!load_runs(a.s_runStart, t, a.s_nbuckets, a.nnz, runPos, runOff) ||
-        runOff[a.s_nbuckets] != e1 - e0) {
-        if (threadIdx.x == 0)
-            flag(a.err);
-        return;
-    }
-    if (emit_runs(runPos, runOff, a.s_nbuckets, e1 - e0, a.s_src, e0, vals, nrows, a.work))
+    } else if (threadIdx.x == 0) {
         flag(a.err);
+    }
+    cluster_barrier<CS>();  // peers may still read this block's slice
 }
 
+// One cluster per bucket of CS * s_bucket_len locals; block r holds locals
+// [r * s_bucket_len, (r+1) * s_bucket_len) of it and places 1/CS of the
+// bucket's work entries (into any block of the cluster).
+template <int CS>
 __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, double *__restrict__ qL)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *out = reinterpret_cast<double *>(smem);
-    const int b = blockIdx.x;
-    const int64_t l0 = static_cast<int64_t>(b) * a.s_bucket_len;
-    const int32_t len = static_cast<int32_t>(
-        a.NL - l0 < a.s_bucket_len ? a.NL - l0 : a.s_bucket_len);
+    const int r = cluster_rank<CS>();
+    const int b = blockIdx.x / CS;
+    const int32_t per = a.s_bucket_len;
+    const int64_t l0 = static_cast<int64_t>(b) * CS * per;
+    const int64_t rest = a.NL - l0;
+    const int32_t len = static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
+    const int32_t mine = max(0, min(per, len - r * per));
     const int32_t j0 = a.s_runStart[b];
     const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + b];
-    if (len <= 0 || j0 < 0 || j1 < j0 || j1 > a.nnz || j1 - j0 > len) {
-        if (threadIdx.x == 0)
-            flag(a.err);
-        return;
-    }
-    for (int32_t i = threadIdx.x; i < len; i += kT)
+    const bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len;
+    for (int32_t i = threadIdx.x; i < mine; i += kT)
         out[i] = 0.0;
-    __syncthreads();
-    bool bad = false;
-    for (int32_t j = j0 + threadIdx.x; j < j1; j += kU * kT) {
-        uint16_t d[kU];
-        double v[kU];
+    double *dst[CS];
+    map_cluster<CS>(out, dst);
+    cluster_barrier<CS>();  // every block's slice is zeroed
+    bool bad = !ok;
+    if (ok) {
+        const int32_t n = j1 - j0;
+        const int32_t jb = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * r / CS);
+        const int32_t je = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * (r + 1) / CS);
+        for (int32_t j = jb + threadIdx.x; j < je; j += kU * kT) {
+            uint16_t d[kU];
+            double v[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int32_t jj = j + u * kT;
-            d[u] = jj < j1 ? ld_u16(a.s_dst + jj) : 0;
-            v[u] = jj < j1 ? ld_seq(a.work + jj) : 0.0;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            if (j + u * kT < j1) {
-                if (d[u] < len)
-                    out[d[u]] = v[u];
-                else
-                    bad = true;
+            for (int u = 0; u < kU; ++u) {
+                const int32_t jj = j + u * kT;
+                d[u] = jj < je ? ld_u16(a.s_dst + jj) : 0;
+                v[u] = jj < je ? ld_seq(a.work + jj) : 0.0;
             }
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (j + u * kT < je) {
+                    if (d[u] < len) {
+                        const int owner = CS == 1 ? 0 : d[u] / per;
+                        pick<CS>(dst, owner)[d[u] - owner * per] = v[u];
+                    } else {
+                        bad = true;
+                    }
+                }
+        }
     }
-    __syncthreads();
-    for (int32_t i = threadIdx.x; i < len; i += kT)
-        qL[l0 + i] = out[i];
-    if (bad)
+    if constexpr (CS == 1)  // the placements are read next by the bulk-copy engine
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    cluster_barrier<CS>();  // every placement has landed
+    const int64_t q0 = l0 + static_cast<int64_t>(r) * per;
+    if (CS == 1 && mine >= 2 && (reinterpret_cast<uintptr_t>(qL + q0) & 15u) == 0) {
+        if (threadIdx.x == 0)
+            bulk_store(qL + q0, out, static_cast<uint32_t>(mine & ~1) * 8u);
+        if ((mine & 1) && threadIdx.x == 32)
+            qL[q0 + mine - 1] = out[mine - 1];
+    } else {
+        for (int32_t i = threadIdx.x; i < mine; i += kT)
+            qL[q0 + i] = out[i];
+    }
+    if (bad && (threadIdx.x == 0 || ok))
         flag(a.err);
 }
 
 // ---------------------------------------------------------------- gather
+// One cluster per tile of CS * g_tile_len locals.
+template <int CS>
 __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const double *__restrict__ qL)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
     int32_t *runPos = reinterpret_cast<int32_t *>(vals + a.g_tile_len);
     int32_t *runOff = runPos + a.g_nbuckets;
-    const int u = blockIdx.x;
-    const int64_t l0 = static_cast<int64_t>(u) * a.g_tile_len;
-    const int32_t len = static_cast<int32_t>(a.NL - l0 < a.g_tile_len ? a.NL - l0 : a.g_tile_len);
+    const int r = cluster_rank<CS>();
+    const int u = blockIdx.x / CS;
+    const int32_t per = a.g_tile_len;
+    const int64_t l0 = static_cast<int64_t>(u) * CS * per;
+    const int64_t rest = a.NL - l0;
+    const int32_t len = static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
     const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
-    if (len <= 0 || s0 < 0 || s1 < s0 || s1 > a.nnz || s1 - s0 > len) {
-        if (threadIdx.x == 0)
-            flag(a.err);
-        return;
+    bool ok = len > 0 && s0 >= 0 && s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0)
+        mbar_init(&bar);
+    __syncthreads();
+    const int32_t m0 = ok ? min(r * per, len) : 0, m1 = ok ? min((r + 1) * per, len) : 0;
+    const bool bulk = stage_start(vals, qL + l0 + m0, m1 - m0, &bar);
+    const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
+    if (!bulk)
+        stage(vals, qL + l0 + m0, m1 - m0);
+    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runPos, runOff) && ok &&
+         runOff[a.g_nbuckets] == s1 - s0;
+    if (bulk && !mbar_wait(&bar)) {
+        ok = false;
+        mbar_wait(&bar);
     }
-    stage(vals, qL + l0, len);
-    if (!load_runs(a.g_runStart, u, a.g_nbuckets, a.nnz, runPos, runOff) ||
-        runOff[a.g_nbuckets] != s1 - s0) {
-        if (threadIdx.x == 0)
+    double *tile[CS];
+    map_cluster<CS>(vals, tile);
+    cluster_barrier<CS>();
+    if (ok) {
+        const int32_t total = s1 - s0;
+        const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
+        const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
+        if (emit_runs<CS>(runPos, runOff, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per, len,
+                          a.work))
             flag(a.err);
-        return;
-    }
-    if (emit_runs(runPos, runOff, a.g_nbuckets, s1 - s0, a.g_src, s0, vals, len, a.work))
+    } else if (threadIdx.x == 0) {
         flag(a.err);
+    }
+    cluster_barrier<CS>();
 }
 
+// One cluster per bucket = CS consecutive sub-buckets of rows; block r
+// holds sub-bucket r, its values staged grouped by row length; it places
+// 1/CS of the bucket's work entries into the owning block, then sums its
+// rows group by group (a warp's lanes all sum rows of the same length) and
+// writes its rows of q_G in order.
+template <int CS>
 __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double *__restrict__ qG)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
-    uint16_t *rs = reinterpret_cast<uint16_t *>(vals + a.g_bucket_entries_max);
-    const int c = blockIdx.x;
-    const int32_t r0 = a.g_bucketRows[c], r1 = a.g_bucketRows[c + 1];
-    const int32_t nrows = r1 - r0;
-    if (r0 < 0 || nrows < 0 || nrows > a.g_bucket_rows_max || r1 > a.NG) {
-        if (threadIdx.x == 0)
-            flag(a.err);
-        return;
+    int32_t *grp = reinterpret_cast<int32_t *>(vals + a.g_bucket_entries_max);  // [mmax+1]
+    __shared__ int32_t rowPre[kMaxRow + 1];
+    __shared__ int grp_bad;
+    const int r = cluster_rank<CS>();
+    const int c = blockIdx.x / CS;
+    const int MM = a.g_mmax;
+    // entry offsets of the CS sub-buckets relative to the bucket start
+    int32_t sub[CS + 1];
+    bool ok = MM >= 1 && MM <= kMaxRow;
+    const int32_t b0 = a.g_subRows[static_cast<int64_t>(c) * CS];
+    ok = ok && b0 >= 0 && b0 <= a.NG;
+    const int32_t E0 = ok ? a.rowStarts[b0] : 0;
+#pragma unroll
+    for (int j = 0; j <= CS; ++j) {
+        const int32_t row = a.g_subRows[static_cast<int64_t>(c) * CS + j];
+        ok = ok && row >= b0 && row <= a.NG;
+        sub[j] = ok ? a.rowStarts[row] - E0 : 0;
+        if (j > 0)
+            ok = ok && sub[j] >= sub[j - 1] && sub[j] - sub[j - 1] <= a.g_bucket_entries_max;
     }
-    const int32_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
-    const int32_t ne = e1 - e0;
+    int32_t mine0 = sub[0], mine1 = sub[1];
+#pragma unroll
+    for (int w = 1; w < CS; ++w)
+        if (r == w) {
+            mine0 = sub[w];
+            mine1 = sub[w + 1];
+        }
+    const int32_t ne = sub[CS], mine = mine1 - mine0;
+    const int64_t sb = static_cast<int64_t>(c) * CS + r;
+    const int32_t r0 = a.g_subRows[sb], r1 = a.g_subRows[sb + 1];
+    const int32_t nrows = r1 - r0;
     const int32_t j0 = a.g_runStart[c];
     const int32_t j1 = a.g_runStart[static_cast<int64_t>(a.g_ntiles) * a.g_nbuckets + c];
-    if (e0 < 0 || ne < 0 || e1 > a.nnz || ne > a.g_bucket_entries_max || j0 != e0 || j1 != e1) {
-        if (threadIdx.x == 0)
-            flag(a.err);
-        return;
+    ok = ok && E0 >= 0 && E0 + ne <= a.nnz && j0 == E0 && j1 == E0 + ne && nrows >= 0 && r1 <= a.NG;
+    if (ok && threadIdx.x <= MM)
+        grp[threadIdx.x] = a.g_groupStart[sb * (MM + 1) + threadIdx.x];
+    if (threadIdx.x == 0) {
+        grp_bad = 0;
+        rowPre[0] = 0;
+    }
+    double *dst[CS];
+    map_cluster<CS>(vals, dst);
+    cluster_barrier<CS>();  // all blocks resident; grp staged
+    if (ok && threadIdx.x == 0) {
+        // rows of length m: (grp[m] - grp[m-1]) / m; rowPre[m] = rows of length <= m
+        int bad = grp[0] != 0 || grp[MM] != mine;
+        int32_t acc = 0;
+        for (int m = 1; m <= MM; ++m) {
+            const int32_t len = grp[m] - grp[m - 1];
+            bad |= len < 0 || len % m != 0;
+            acc += len / m;
+            rowPre[m] = acc;
+        }
+        bad |= acc > nrows;
+        grp_bad = bad;
     }
     bool bad = false;
-    for (int32_t j = threadIdx.x; j < ne; j += kU * kT) {
-        uint16_t p[kU];
-        double v[kU];
+    if (ok) {
+        const int32_t jb = static_cast<int32_t>(static_cast<int64_t>(ne) * r / CS);
+        const int32_t je = static_cast<int32_t>(static_cast<int64_t>(ne) * (r + 1) / CS);
+        for (int32_t j = jb + threadIdx.x; j < je; j += kU * kT) {
+            uint16_t p[kU];
+            double v[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-            const int32_t jj = j + u * kT;
-            p[u] = jj < ne ? ld_u16(a.g_pos + e0 + jj) : 0;
-            v[u] = jj < ne ? ld_seq(a.work + e0 + jj) : 0.0;
+            for (int q = 0; q < kU; ++q) {
+                const int32_t jj = j + q * kT;
+                p[q] = jj < je ? ld_u16(a.g_pos + E0 + jj) : 0;
+                v[q] = jj < je ? ld_seq(a.work + E0 + jj) : 0.0;
+            }
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+                if (j + q * kT < je) {
+                    if (p[q] < ne) {
+                        int owner = 0;
+                        int32_t base = sub[0];
+#pragma unroll
+                        for (int w = 1; w < CS; ++w) {
+                            owner += p[q] >= sub[w];
+                            base = p[q] >= sub[w] ? sub[w] : base;
+                        }
+                        pick<CS>(dst, owner)[p[q] - base] = v[q];
+                    } else {
+                        bad = true;
+                    }
+                }
         }
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            if (j + u * kT < ne) {
-                if (p[u] < ne)
-                    vals[p[u]] = v[u];
-                else
-                    bad = true;
-            }
     }
-    for (int32_t k0 = threadIdx.x; k0 <= nrows; k0 += kU * kT) {
-        int32_t o[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            o[u] = k0 + u * kT <= nrows ? a.rowStarts[r0 + k0 + u * kT] - e0 : 0;
-#pragma unroll
-        for (int u = 0; u < kU; ++u)
-            if (k0 + u * kT <= nrows) {
-                if (o[u] < 0 || o[u] > ne)
-                    bad = true;
-                rs[k0 + u * kT] = static_cast<uint16_t>(o[u] < 0 ? 0 : (o[u] > ne ? ne : o[u]));
-            }
+    cluster_barrier<CS>();  // every placement has landed; rowPre ready
+    const bool go = ok && grp_bad == 0;
+    if (go) {
+        // sums in the grouped layout, in place into each row's first slot
+        const int32_t R = rowPre[MM];
+        for (int32_t q = threadIdx.x; q < R; q += kT) {
+            int m = 1;
+            while (m < MM && rowPre[m] <= q)
+                ++m;
+            const int32_t base = grp[m - 1] + (q - rowPre[m - 1]) * m;
+            vals[base] = row_sum(vals + base, m);
+        }
     }
     __syncthreads();
-    for (int32_t k = threadIdx.x; k < nrows; k += kT) {
-        const int32_t lo = rs[k], hi = rs[k + 1];
-        if (hi < lo)
-            bad = true;
-        qG[r0 + k] = hi > lo ? row_sum(vals + lo, hi - lo) : 0.0;
+    if (go) {
+        for (int32_t k0 = threadIdx.x; k0 < nrows; k0 += kU * kT) {
+            uint16_t p[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+                p[q] = k0 + q * kT < nrows ? ld_u16(a.g_rowPos + r0 + k0 + q * kT) : 0;
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+                if (k0 + q * kT < nrows) {
+                    double v = 0.0;
+                    if (p[q] != 0xFFFF) {
+                        if (p[q] < mine)
+                            v = vals[p[q]];
+                        else
+                            bad = true;
+                    }
+                    qG[r0 + k0 + q * kT] = v;
+                }
+        }
     }
-    if (bad)
+    if (bad || (!go && threadIdx.x == 0))
         flag(a.err);
 }
 
 int64_t smem_s1(const bs_plan_dev *p) { return 8ll * p->s_tile_rows + 4ll * p->s_nbuckets + 4ll * (p->s_nbuckets + 1); }
 int64_t smem_s2(const bs_plan_dev *p) { return 8ll * p->s_bucket_len; }
 int64_t smem_g1(const bs_plan_dev *p) { return 8ll * p->g_tile_len + 4ll * p->g_nbuckets + 4ll * (p->g_nbuckets + 1); }
-int64_t smem_g2(const bs_plan_dev *p) { return 8ll * p->g_bucket_entries_max + 2ll * (p->g_bucket_rows_max + 1); }
+int64_t smem_g2(const bs_plan_dev *p) { return 8ll * p->g_bucket_entries_max + 4ll * (kMaxRow + 1); }
 
 constexpr int64_t kSmemMax = 232448;
 
-template <class K>
-int set_smem(bs_ctx *ctx, K kernel, int64_t bytes)
+template <class... KArgs, class... Args>
+int launch(bs_ctx *ctx, const char *name, void (*kernel)(KArgs...), int cs, int64_t clusters,
+           int64_t smem, cudaStream_t s, Args... args)
 {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
+                                         static_cast<int>(smem));
     if (e != cudaSuccess)
-        return bs_set_error(ctx, BS_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        return bs_set_error(ctx, BS_ECUDA, "%s: cudaFuncSetAttribute: %s", name,
+                            cudaGetErrorString(e));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cs), 1, 1);
+    cfg.blockDim = dim3(kT, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cs > 1 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess)
+        return bs_set_error(ctx, BS_ECUDA, "launch of %s: %s", name, cudaGetErrorString(e));
     return BS_OK;
 }
 
@@ -407,18 +711,28 @@ int check_plan(bs_ctx *ctx, const char *name, const bs_gs_dev *t, const void *qL
     const bs_plan_dev *p = t->plan;
     if (!t->rowStarts)
         return bs_set_error(ctx, BS_EINVAL, "%s: the plan needs rowStarts", name);
+    if (p->cluster != 1 && p->cluster != 2 && p->cluster != 4)
+        return bs_set_error(ctx, BS_EINVAL, "%s: plan cluster size must be 1, 2 or 4", name);
     if (p->s_ntiles < 1 || p->s_nbuckets < 1 || p->s_tile_rows < 1 || p->s_bucket_len < 1 ||
         p->g_ntiles < 1 || p->g_nbuckets < 1 || p->g_tile_len < 1 || p->g_bucket_entries_max < 1 ||
         p->g_bucket_rows_max < 1)
         return bs_set_error(ctx, BS_EINVAL, "%s: bad plan sizes", name);
-    if (static_cast<int64_t>(p->s_nbuckets) * p->s_bucket_len < t->NL ||
-        static_cast<int64_t>(p->g_ntiles) * p->g_tile_len < t->NL)
+    const int64_t cs = p->cluster;
+    if (cs * p->s_tile_rows > 65536 || cs * p->s_bucket_len > 65536 ||
+        cs * p->g_tile_len > 65536 || cs * p->g_bucket_entries_max > 65535)
+        return bs_set_error(ctx, BS_EINVAL, "%s: plan offsets exceed 16 bits", name);
+    if (cs * p->s_nbuckets * p->s_bucket_len < t->NL || cs * p->g_ntiles * p->g_tile_len < t->NL ||
+        cs * p->s_ntiles * p->s_tile_rows < t->NG)
         return bs_set_error(ctx, BS_EINVAL, "%s: plan does not cover the mesh", name);
     if (smem_s1(p) > kSmemMax || smem_s2(p) > kSmemMax || smem_g1(p) > kSmemMax ||
         smem_g2(p) > kSmemMax)
         return bs_set_error(ctx, BS_EINVAL, "%s: plan needs too much shared memory", name);
-    if (!p->s_tileRows || !p->s_runStart || !p->g_bucketRows || !p->g_tileSlot ||
-        !p->g_runStart || !p->work || (t->nnz > 0 && (!p->s_src || !p->s_dst || !p->g_src || !p->g_pos)))
+    if (p->g_mmax < 1 || p->g_mmax > kMaxRow)
+        return bs_set_error(ctx, BS_EINVAL, "%s: plan row length bound outside [1, %d]", name,
+                            kMaxRow);
+    if (!p->s_tileRows || !p->s_runStart || !p->g_subRows || !p->g_tileSlot ||
+        !p->g_runStart || !p->work || !p->g_groupStart || !p->g_rowPos ||
+        (t->nnz > 0 && (!p->s_src || !p->s_dst || !p->g_src || !p->g_pos)))
         return bs_set_error(ctx, BS_EINVAL, "%s: NULL plan table", name);
     if (p->work_len < t->nnz)
         return bs_set_error(ctx, BS_EINVAL, "%s: work buffer shorter than nnz", name);
@@ -446,19 +760,44 @@ PlanArgs make_args(const bs_ctx *ctx, const bs_gs_dev *t)
     a.g_tile_len = p->g_tile_len;
     a.g_bucket_entries_max = p->g_bucket_entries_max;
     a.g_bucket_rows_max = p->g_bucket_rows_max;
+    a.g_mmax = p->g_mmax;
     a.rowStarts = t->rowStarts;
     a.s_tileRows = p->s_tileRows;
     a.s_runStart = p->s_runStart;
     a.s_src = p->s_src;
     a.s_dst = p->s_dst;
-    a.g_bucketRows = p->g_bucketRows;
+    a.g_subRows = p->g_subRows;
     a.g_tileSlot = p->g_tileSlot;
     a.g_runStart = p->g_runStart;
     a.g_src = p->g_src;
     a.g_pos = p->g_pos;
+    a.g_groupStart = p->g_groupStart;
+    a.g_rowPos = p->g_rowPos;
     a.work = p->work;
     a.err = ctx->dev_err;
     return a;
+}
+
+template <int CS>
+int scatter_cs(bs_ctx *ctx, const PlanArgs &a, const bs_plan_dev *p, const double *qG, double *qL,
+               cudaStream_t s)
+{
+    if (int st = launch(ctx, "scatter_tile_kernel", scatter_tile_kernel<CS>, CS, p->s_ntiles,
+                        smem_s1(p), s, a, qG))
+        return st;
+    return launch(ctx, "scatter_bucket_kernel", scatter_bucket_kernel<CS>, CS, p->s_nbuckets,
+                  smem_s2(p), s, a, qL);
+}
+
+template <int CS>
+int gather_cs(bs_ctx *ctx, const PlanArgs &a, const bs_plan_dev *p, const double *qL, double *qG,
+              cudaStream_t s)
+{
+    if (int st = launch(ctx, "gather_tile_kernel", gather_tile_kernel<CS>, CS, p->g_ntiles,
+                        smem_g1(p), s, a, qL))
+        return st;
+    return launch(ctx, "gather_bucket_kernel", gather_bucket_kernel<CS>, CS, p->g_nbuckets,
+                  smem_g2(p), s, a, qG);
 }
 
 } // namespace
@@ -470,15 +809,11 @@ int bs_scatter_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, double
         return st;
     const bs_plan_dev *p = t->plan;
     const PlanArgs a = make_args(ctx, t);
-    if (int st = set_smem(ctx, scatter_tile_kernel, smem_s1(p)))
-        return st;
-    if (int st = set_smem(ctx, scatter_bucket_kernel, smem_s2(p)))
-        return st;
-    scatter_tile_kernel<<<p->s_ntiles, kT, smem_s1(p), s>>>(a, qG);
-    BS_LAUNCH_CHECK(ctx, "scatter_tile_kernel");
-    scatter_bucket_kernel<<<p->s_nbuckets, kT, smem_s2(p), s>>>(a, qL);
-    BS_LAUNCH_CHECK(ctx, "scatter_bucket_kernel");
-    return BS_OK;
+    switch (p->cluster) {
+    case 1: return scatter_cs<1>(ctx, a, p, qG, qL, s);
+    case 2: return scatter_cs<2>(ctx, a, p, qG, qL, s);
+    default: return scatter_cs<4>(ctx, a, p, qG, qL, s);
+    }
 }
 
 int bs_gather_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double *qG,
@@ -488,13 +823,9 @@ int bs_gather_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double 
         return st;
     const bs_plan_dev *p = t->plan;
     const PlanArgs a = make_args(ctx, t);
-    if (int st = set_smem(ctx, gather_tile_kernel, smem_g1(p)))
-        return st;
-    if (int st = set_smem(ctx, gather_bucket_kernel, smem_g2(p)))
-        return st;
-    gather_tile_kernel<<<p->g_ntiles, kT, smem_g1(p), s>>>(a, qL);
-    BS_LAUNCH_CHECK(ctx, "gather_tile_kernel");
-    gather_bucket_kernel<<<p->g_nbuckets, kT, smem_g2(p), s>>>(a, qG);
-    BS_LAUNCH_CHECK(ctx, "gather_bucket_kernel");
-    return BS_OK;
+    switch (p->cluster) {
+    case 1: return gather_cs<1>(ctx, a, p, qL, qG, s);
+    case 2: return gather_cs<2>(ctx, a, p, qL, qG, s);
+    default: return gather_cs<4>(ctx, a, p, qL, qG, s);
+    }
 }

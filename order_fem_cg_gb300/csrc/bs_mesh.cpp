@@ -204,7 +204,8 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
         seg_max = std::max<int32_t>(seg_max, static_cast<int32_t>(std::max(ce, cr)));
         m->blockStarts.push_back(static_cast<int32_t>(NG));
         m->seg_max = std::max<int32_t>(seg_max, 1);
-        bs_plan_build(m, BS_TILE_S_ROWS, BS_TILE_S_BUCKET, BS_TILE_G_LOCALS, BS_TILE_G_BUCKET);
+        bs_plan_build(m, BS_TILE_S_ROWS, BS_TILE_S_BUCKET, BS_TILE_G_LOCALS, BS_TILE_G_BUCKET,
+                      BS_TILE_CLUSTER);
     } catch (const std::bad_alloc &) {
         delete m;
         return BS_ENOMEM;
@@ -307,12 +308,12 @@ extern "C" int bs_mesh_destroy(bs_mesh *m)
 }
 
 extern "C" int bs_mesh_plan(bs_mesh *m, int32_t s_tile_rows, int32_t s_bucket_len,
-                            int32_t g_tile_len, int32_t g_bucket_entries)
+                            int32_t g_tile_len, int32_t g_bucket_entries, int32_t cluster)
 {
     if (!m)
         return BS_EINVAL;
     try {
-        bs_plan_build(m, s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries);
+        bs_plan_build(m, s_tile_rows, s_bucket_len, g_tile_len, g_bucket_entries, cluster);
     } catch (const std::bad_alloc &) {
         m->plan = bs_plan();
         return BS_ENOMEM;
@@ -327,6 +328,7 @@ extern "C" int bs_mesh_plan_info(const bs_mesh *m, bs_plan_info_t *out)
     const bs_plan &p = m->plan;
     std::memset(out, 0, sizeof(*out));
     out->valid = p.valid ? 1 : 0;
+    out->cluster = p.cluster;
     out->s_tile_rows = p.s_tile_rows;
     out->s_bucket_len = p.s_bucket_len;
     out->g_tile_len = p.g_tile_len;
@@ -337,6 +339,7 @@ extern "C" int bs_mesh_plan_info(const bs_mesh *m, bs_plan_info_t *out)
     out->g_nbuckets = p.g_nbuckets;
     out->g_bucket_rows_max = p.g_bucket_rows_max;
     out->g_bucket_entries_max = p.g_bucket_entries_max;
+    out->g_mmax = p.g_mmax;
     if (p.valid) {
         out->smem_s1 = bs_plan_smem_s1(p);
         out->smem_s2 = bs_plan_smem_s2(p);
@@ -348,9 +351,10 @@ extern "C" int bs_mesh_plan_info(const bs_mesh *m, bs_plan_info_t *out)
 
 extern "C" int bs_mesh_plan_tables(const bs_mesh *m, const int32_t **s_tileRows,
                                    const int32_t **s_runStart, const uint16_t **s_src,
-                                   const uint16_t **s_dst, const int32_t **g_bucketRows,
+                                   const uint16_t **s_dst, const int32_t **g_subRows,
                                    const int32_t **g_tileSlot, const int32_t **g_runStart,
-                                   const uint16_t **g_src, const uint16_t **g_pos)
+                                   const uint16_t **g_src, const uint16_t **g_pos,
+                                   const uint16_t **g_groupStart, const uint16_t **g_rowPos)
 {
     if (!m || !m->plan.valid)
         return BS_EINVAL;
@@ -359,10 +363,12 @@ extern "C" int bs_mesh_plan_tables(const bs_mesh *m, const int32_t **s_tileRows,
     if (s_runStart) *s_runStart = p.s_runStart.data();
     if (s_src) *s_src = p.s_src.data();
     if (s_dst) *s_dst = p.s_dst.data();
-    if (g_bucketRows) *g_bucketRows = p.g_bucketRows.data();
+    if (g_subRows) *g_subRows = p.g_subRows.data();
     if (g_tileSlot) *g_tileSlot = p.g_tileSlot.data();
     if (g_runStart) *g_runStart = p.g_runStart.data();
     if (g_src) *g_src = p.g_src.data();
     if (g_pos) *g_pos = p.g_pos.data();
+    if (g_groupStart) *g_groupStart = p.g_groupStart.data();
+    if (g_rowPos) *g_rowPos = p.g_rowPos.data();
     return BS_OK;
 }

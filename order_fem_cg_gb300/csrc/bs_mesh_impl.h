@@ -18,20 +18,39 @@
 // places a bucket's values by CSR position and sums each row in ascending
 // local order.  The work array is ordered bucket-major, then tile, so both
 // passes touch it in runs.
+//
+// Each tile and bucket is handled by a cluster of `cluster` thread blocks
+// whose shared memories together hold it (distributed shared memory), so
+// a tile is cluster x the per-block size; runs grow with tile x bucket.
+// A gather bucket is `cluster` consecutive sub-buckets, each a row range
+// of at most g_bucket_entries entries and rows held by one block.  Inside a
+// sub-bucket the values are staged grouped by row length m (all rows with
+// m entries together, m values per row, rows and their values in ascending
+// order), so that a warp sums rows of equal length with all lanes busy --
+// a binary64 warp instruction holds the SM's FP64 pipe for ~20 cycles on
+// GB300 however many lanes are active.
+// Sizes below are per block.
 struct bs_plan {
     bool valid = false;
+    int32_t cluster = 1;
     int32_t s_tile_rows = 0, s_bucket_len = 0, g_tile_len = 0, g_bucket_entries = 0;
     int32_t s_ntiles = 0, s_nbuckets = 0, g_ntiles = 0, g_nbuckets = 0;
-    int32_t g_bucket_rows_max = 0, g_bucket_entries_max = 0;
+    int32_t g_bucket_rows_max = 0, g_bucket_entries_max = 0;  // per sub-bucket
+    int32_t g_mmax = 0;                                       // longest row
     std::vector<int32_t> s_tileRows;   // [s_ntiles+1]  first row of each scatter tile
     std::vector<int32_t> s_runStart;   // [(s_ntiles+1) x s_nbuckets] work position of run (t, b)
     std::vector<uint16_t> s_src;       // [nnz] tile-major: row offset within the tile
     std::vector<uint16_t> s_dst;       // [nnz] work order: local offset within the bucket
-    std::vector<int32_t> g_bucketRows; // [g_nbuckets+1] first row of each gather bucket
+    std::vector<int32_t> g_subRows;    // [cluster x g_nbuckets + 1] first row of each sub-bucket
     std::vector<int32_t> g_tileSlot;   // [g_ntiles+1]  unmasked locals before each tile
     std::vector<int32_t> g_runStart;   // [(g_ntiles+1) x g_nbuckets]
     std::vector<uint16_t> g_src;       // [nnz] tile-major: local offset within the tile
-    std::vector<uint16_t> g_pos;       // [nnz] work order: CSR position within the bucket
+    std::vector<uint16_t> g_pos;       // [nnz] work order: staged position within the bucket
+    std::vector<uint16_t> g_groupStart; // [cluster x g_nbuckets x (g_mmax+1)] per sub-bucket:
+                                        // [m-1] = first position of the rows of length m,
+                                        // [g_mmax] = entries of the sub-bucket
+    std::vector<uint16_t> g_rowPos;    // [NG] staged position of a row's first value within
+                                       // its sub-bucket, 0xFFFF for a row without entries
 };
 
 struct bs_mesh {
@@ -43,8 +62,11 @@ struct bs_mesh {
     bs_plan plan;
 };
 
-// Default plan sizes: each fills most of a GB300 SM's 227 KB of shared
-// memory (8 bytes per staged value).
+// Default plan: one block per tile or bucket (clusters of 2 and 4 measured
+// slower on GB300: random 8-byte accesses to a peer block's shared memory
+// cost more than the longer runs save), each block filling most of a GB300
+// SM's 227 KB of shared memory (8 bytes per staged value).
+constexpr int32_t BS_TILE_CLUSTER = 1;
 constexpr int32_t BS_TILE_S_ROWS = 24576;
 constexpr int32_t BS_TILE_S_BUCKET = 24576;
 constexpr int32_t BS_TILE_G_LOCALS = 24576;
@@ -57,8 +79,10 @@ int64_t bs_plan_smem_s1(const bs_plan &p);
 int64_t bs_plan_smem_s2(const bs_plan &p);
 int64_t bs_plan_smem_g1(const bs_plan &p);
 int64_t bs_plan_smem_g2(const bs_plan &p);
+// Longest row the grouped gather supports.
+constexpr int32_t BS_PLAN_MMAX = 32;
 
 // (Re)builds m->plan; leaves it invalid (empty) when a kernel would need
 // more shared memory than a block can have.  Throws std::bad_alloc.
 void bs_plan_build(bs_mesh *m, int32_t s_tile_rows, int32_t s_bucket_len, int32_t g_tile_len,
-                   int32_t g_bucket_entries);
+                   int32_t g_bucket_entries, int32_t cluster);

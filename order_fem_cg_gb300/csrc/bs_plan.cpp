@@ -26,26 +26,32 @@ int64_t bs_plan_smem_g1(const bs_plan &p)
 
 int64_t bs_plan_smem_g2(const bs_plan &p)
 {
-    // staged values, then 16-bit row offsets
-    return 8ll * p.g_bucket_entries_max + 2ll * (p.g_bucket_rows_max + 1);
+    // staged values, then the sub-bucket's group table
+    return 8ll * p.g_bucket_entries_max + 4ll * (BS_PLAN_MMAX + 1);
 }
 
-void bs_plan_build(bs_mesh *m, int32_t TR, int32_t BL, int32_t TL, int32_t EB)
+void bs_plan_build(bs_mesh *m, int32_t TRc, int32_t BLc, int32_t TLc, int32_t EBc, int32_t CS)
 {
     m->plan = bs_plan();
     bs_plan &p = m->plan;
-    // offsets inside a tile or bucket are stored as 16 bits
-    if (TR < 1 || BL < 1 || TL < 1 || EB < 8 || TR > 65536 || BL > 65536 || TL > 65536 ||
-        EB > 65535)
+    if (CS != 1 && CS != 2 && CS != 4)
+        return;
+    // offsets inside a tile or bucket (whole cluster) are stored as 16 bits
+    if (TRc < 1 || BLc < 1 || TLc < 1 || EBc < 8 || static_cast<int64_t>(TRc) * CS > 65536 ||
+        static_cast<int64_t>(BLc) * CS > 65536 || static_cast<int64_t>(TLc) * CS > 65536 ||
+        static_cast<int64_t>(EBc) * CS > 65535)
         return;
     const int64_t NL = m->NL, NG = m->NG, nnz = m->nnz;
     const int32_t *rs = m->rowStarts.data();
     const int32_t *li = m->localIds.data();
     const int32_t *ids = m->scatterIds.data();
-    p.s_tile_rows = TR;
-    p.s_bucket_len = BL;
-    p.g_tile_len = TL;
-    p.g_bucket_entries = EB;
+    p.cluster = CS;
+    p.s_tile_rows = TRc;
+    p.s_bucket_len = BLc;
+    p.g_tile_len = TLc;
+    p.g_bucket_entries = EBc;
+    const int64_t TR = static_cast<int64_t>(TRc) * CS, BL = static_cast<int64_t>(BLc) * CS;
+    const int64_t TL = static_cast<int64_t>(TLc) * CS;
 
     // ------------------------------------------------------------ scatter
     const int64_t T = (NG + TR - 1) / TR, B = (NL + BL - 1) / BL;
@@ -100,39 +106,74 @@ void bs_plan_build(bs_mesh *m, int32_t TR, int32_t BL, int32_t TL, int32_t EB)
     // ------------------------------------------------------------- gather
     const int64_t U = (NL + TL - 1) / TL;
     p.g_ntiles = static_cast<int32_t>(U);
-    // buckets: consecutive rows, at most EB entries and EB rows each
-    p.g_bucketRows.clear();
-    p.g_bucketRows.push_back(0);
-    std::vector<int32_t> bucketOf(NG);
+    // sub-buckets: consecutive rows, at most EBc entries and EBc rows each;
+    // a bucket is CS consecutive sub-buckets (padded with empty ones)
+    std::vector<int32_t> subOf(NG);
+    p.g_subRows.clear();
+    p.g_subRows.push_back(0);
     {
         int64_t ce = 0, cr = 0;
         int32_t emax = 0, rmax = 0;
         for (int64_t g = 0; g < NG; ++g) {
             const int64_t len = rs[g + 1] - rs[g];
-            if (cr > 0 && (ce + len > EB || cr + 1 > EB)) {
-                p.g_bucketRows.push_back(static_cast<int32_t>(g));
+            if (cr > 0 && (ce + len > EBc || cr + 1 > EBc)) {
+                p.g_subRows.push_back(static_cast<int32_t>(g));
                 emax = std::max<int32_t>(emax, static_cast<int32_t>(ce));
                 rmax = std::max<int32_t>(rmax, static_cast<int32_t>(cr));
                 ce = 0;
                 cr = 0;
             }
-            bucketOf[g] = static_cast<int32_t>(p.g_bucketRows.size()) - 1;
+            subOf[g] = static_cast<int32_t>(p.g_subRows.size()) - 1;
             ce += len;
             cr += 1;
         }
         emax = std::max<int32_t>(emax, static_cast<int32_t>(ce));
         rmax = std::max<int32_t>(rmax, static_cast<int32_t>(cr));
-        p.g_bucketRows.push_back(static_cast<int32_t>(NG));
+        p.g_subRows.push_back(static_cast<int32_t>(NG));
+        while ((p.g_subRows.size() - 1) % CS != 0)
+            p.g_subRows.push_back(static_cast<int32_t>(NG));
         p.g_bucket_entries_max = std::max<int32_t>(emax, 1);
         p.g_bucket_rows_max = std::max<int32_t>(rmax, 1);
     }
-    const int64_t C = static_cast<int64_t>(p.g_bucketRows.size()) - 1;
+    const int64_t C = (static_cast<int64_t>(p.g_subRows.size()) - 1) / CS;
     p.g_nbuckets = static_cast<int32_t>(C);
     if (bs_plan_smem_g1(p) > BS_SMEM_MAX || bs_plan_smem_g2(p) > BS_SMEM_MAX ||
         static_cast<double>(U + 1) * C > 2e9) {
         m->plan = bs_plan();
         return;
     }
+    // rows grouped by length inside each sub-bucket
+    const int32_t MM = std::max<int32_t>(m->max_row, 1);
+    if (MM > BS_PLAN_MMAX) {
+        m->plan = bs_plan();
+        return;
+    }
+    p.g_mmax = MM;
+    const int64_t NS = static_cast<int64_t>(p.g_subRows.size()) - 1;
+    p.g_groupStart.assign(static_cast<size_t>(NS) * (MM + 1), 0);
+    p.g_rowPos.assign(NG, 0xFFFF);
+    for (int64_t sb = 0; sb < NS; ++sb) {
+        uint16_t *gs = p.g_groupStart.data() + sb * (MM + 1);
+        int32_t cnt[BS_PLAN_MMAX + 1] = {0};
+        for (int32_t g = p.g_subRows[sb]; g < p.g_subRows[sb + 1]; ++g)
+            ++cnt[rs[g + 1] - rs[g]];
+        int32_t acc = 0, next[BS_PLAN_MMAX + 1];
+        for (int32_t len = 1; len <= MM; ++len) {
+            gs[len - 1] = static_cast<uint16_t>(acc);
+            next[len] = acc;
+            acc += cnt[len] * len;
+        }
+        gs[MM] = static_cast<uint16_t>(acc);
+        for (int32_t g = p.g_subRows[sb]; g < p.g_subRows[sb + 1]; ++g) {
+            const int32_t len = rs[g + 1] - rs[g];
+            if (len > 0) {
+                p.g_rowPos[g] = static_cast<uint16_t>(next[len]);
+                next[len] += len;
+            }
+        }
+    }
+    // staged position of CSR entry e (row g, k-th entry) within its bucket:
+    // offset of its sub-bucket in the bucket + grouped position of the row + k
     std::vector<int32_t> epos(NL, -1);
     for (int64_t e = 0; e < nnz; ++e)
         epos[li[e]] = static_cast<int32_t>(e);
@@ -151,12 +192,12 @@ void bs_plan_build(bs_mesh *m, int32_t TR, int32_t BL, int32_t TL, int32_t EB)
         std::vector<int32_t> cnt(static_cast<size_t>(U) * C, 0);
         for (int64_t l = 0; l < NL; ++l)
             if (ids[l] >= 0)
-                ++cnt[(l / TL) * C + bucketOf[ids[l]]];
+                ++cnt[(l / TL) * C + subOf[ids[l]] / CS];
         // work order: bucket-major (a bucket's range is its CSR range), then
         // tile, then ascending local id
         p.g_runStart.resize(static_cast<size_t>(U + 1) * C);
         for (int64_t c = 0; c < C; ++c) {
-            int64_t pos = rs[p.g_bucketRows[c]];
+            int64_t pos = rs[p.g_subRows[c * CS]];
             for (int64_t u = 0; u < U; ++u) {
                 p.g_runStart[u * C + c] = static_cast<int32_t>(pos);
                 pos += cnt[u * C + c];
@@ -179,11 +220,13 @@ void bs_plan_build(bs_mesh *m, int32_t TR, int32_t BL, int32_t TL, int32_t EB)
                 const int32_t g = ids[l];
                 if (g < 0)
                     continue;
-                const int64_t c = bucketOf[g];
+                const int64_t c = subOf[g] / CS;
                 const int32_t k = cur[c]++;
                 p.g_src[base + off[c] + k] = static_cast<uint16_t>(l - l0);
+                const int64_t sb = subOf[g];
+                const int64_t in_bucket = rs[p.g_subRows[sb]] - rs[p.g_subRows[c * CS]];
                 p.g_pos[p.g_runStart[u * C + c] + k] =
-                    static_cast<uint16_t>(epos[l] - rs[p.g_bucketRows[c]]);
+                    static_cast<uint16_t>(in_bucket + p.g_rowPos[g] + (epos[l] - rs[g]));
             }
         }
     }

@@ -152,6 +152,104 @@ __device__ __forceinline__ void finish_reduction(double v, const RedOut &o)
     }
 }
 
+// ------------------------------------------- sums of squares off the FP64 pipe
+// GB300 runs binary64 fma/add at ~1.6 per clock per SM, so a sum of
+// squares with one fma per element is bound by the FP64 pipe below HBM
+// speed.  SqAcc forms x^2 and sums it on the FP32 and integer pipes:
+//   |x| = xh + xl with xh the leading 24 significant bits (a float, exact)
+//   and xl the next 23 bits (exact float; the last 6 bits are dropped,
+//   an error below 2^-46 |x|), built with integer and FP32 operations only
+//   (on this part int<->float conversions are as scarce as FP64 math);
+//   x^2 ~= xh^2 + (2 xh xl + xl^2), xh^2 exact as p + e (TwoProduct by
+//   fmaf); p is added to a float-float sum (s, c) by TwoSum, the small
+//   terms to c.  Every flush (8 elements) moves (s, c) into a binary64 total
+//   with an exact float->double conversion done on the integer pipe.
+// Per element the relative error is <= ~2^-45; per 8-element chunk the
+// float accumulation adds <= ~2^-40; all terms are >= 0, so the total
+// stays within 1e-12 relative.  |x| outside [2^-40, 2^41) (subnormal,
+// tiny, huge, inf, NaN) goes through a separate binary64 fma sum instead.
+constexpr uint32_t kSqExpLo = 1023 - 40, kSqExpHi = 1023 + 40;
+
+__device__ __forceinline__ double float_to_double_exact(float f)
+{
+    const uint32_t b = __float_as_uint(f);
+    const uint32_t mag = b & 0x7FFFFFFFu;
+    if ((mag >> 23) == 0)  // zero or subnormal: far below the running sum
+        return 0.0;
+    const uint32_t hi = (b & 0x80000000u) | ((mag >> 3) + ((1023u - 127u) << 20));
+    return __hiloint2double(static_cast<int>(hi), static_cast<int>(mag << 29));
+}
+
+struct SqAcc {
+    float s, c;   // float-float partial sum of the current chunk
+    double d;     // flushed chunks
+    double slow;  // out-of-range terms
+
+    __device__ __forceinline__ void init()
+    {
+        s = 0.f;
+        c = 0.f;
+        d = 0.0;
+        slow = 0.0;
+    }
+
+    // Adds x^2 if |x| is in the fast range or x is 0; otherwise only marks
+    // the lane (`pending`): the caller re-walks its elements with add_slow
+    // afterwards.  No binary64 math on this path -- an issued fma holds the
+    // FP64 pipe for the whole warp even when predicated off.
+    __device__ __forceinline__ void add(double x, bool &pending)
+    {
+        const uint32_t hw = static_cast<uint32_t>(__double2hiint(x)) & 0x7FFFFFFFu;
+        const uint32_t lw = static_cast<uint32_t>(__double2loint(x));
+        const uint32_t E = hw >> 20;
+        const bool fast = E - kSqExpLo <= kSqExpHi - kSqExpLo;
+        pending |= !fast && (hw | lw) != 0;
+        if (fast) {
+            const uint32_t t = hw - ((1023u - 127u) << 20);
+            const float xh = __uint_as_float(__funnelshift_l(lw, t, 3));
+            // xl: bits 6..28 of the fraction as an exact float (2^23 + k) - 2^23,
+            // scaled by 2^(e-46); the 6 dropped bits are below 2^-46 |x|.
+            const float k23 = __fsub_rn(
+                __uint_as_float(0x4B000000u | ((lw & 0x1FFFFFFFu) >> 6)), 8388608.0f);
+            const float scale = __uint_as_float((E - (1023u + 46u - 127u)) << 23);
+            const float xl = __fmul_rn(k23, scale);
+            const float p = __fmul_rn(xh, xh);
+            float q = __fmaf_rn(xh, xh, -p);
+            q = __fmaf_rn(__fadd_rn(xh, xh), xl, q);
+            q = __fmaf_rn(xl, xl, q);
+            const float sn = __fadd_rn(s, p);
+            const float bp = __fsub_rn(sn, s);
+            const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(sn, bp)), __fsub_rn(p, bp));
+            s = sn;
+            c = __fadd_rn(c, __fadd_rn(err, q));
+        }
+    }
+
+    // The second walk: x^2 of the out-of-range values only, in binary64.
+    __device__ __forceinline__ void add_slow(double x)
+    {
+        const uint32_t hw = static_cast<uint32_t>(__double2hiint(x)) & 0x7FFFFFFFu;
+        const uint32_t lw = static_cast<uint32_t>(__double2loint(x));
+        const uint32_t E = hw >> 20;
+        if (!(E - kSqExpLo <= kSqExpHi - kSqExpLo) && (hw | lw) != 0)
+            slow = __fma_rn(x, x, slow);
+    }
+
+    __device__ __forceinline__ void flush()
+    {
+        d = __dadd_rn(d, float_to_double_exact(s));
+        d = __dadd_rn(d, float_to_double_exact(c));
+        s = 0.f;
+        c = 0.f;
+    }
+
+    __device__ __forceinline__ double total()
+    {
+        flush();
+        return __dadd_rn(d, slow);
+    }
+};
+
 // ---------------------------------------------------------------- BS1 copy
 template <int V, int UNROLL>
 __global__ void __launch_bounds__(kThreads) copy_kernel(const double *__restrict__ x,
@@ -227,9 +325,12 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const double *__restrict_
     const double *xv = x + h;
     const double *yv = y + h;
     double acc[V];
+    SqAcc sq;
+    bool pending = false;
 #pragma unroll
     for (int k = 0; k < V; ++k)
         acc[k] = 0.0;
+    sq.init();
     for (int64_t b = gid; b < nv; b += stride * UNROLL) {
         Vec<V> a[UNROLL], c[UNROLL];
 #pragma unroll
@@ -243,18 +344,39 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const double *__restrict_
         for (int u = 0; u < UNROLL; ++u)
             if (b + u * stride < nv) {
 #pragma unroll
-                for (int k = 0; k < V; ++k)
-                    acc[k] = __fma_rn(a[u].v[k], DOT ? c[u].v[k] : a[u].v[k], acc[k]);
+                for (int k = 0; k < V; ++k) {
+                    if (DOT)
+                        acc[k] = __fma_rn(a[u].v[k], c[u].v[k], acc[k]);
+                    else
+                        sq.add(a[u].v[k], pending);
+                }
             }
+        if (!DOT)
+            sq.flush();
     }
     if (gid < h + t) {
         const int64_t i = scalar_index(gid, h, nv, V);
-        acc[0] = __fma_rn(x[i], DOT ? y[i] : x[i], acc[0]);
+        if (DOT)
+            acc[0] = __fma_rn(x[i], y[i], acc[0]);
+        else
+            sq.add(x[i], pending);
     }
-    double s = acc[0];
+    if (!DOT && pending) {  // this thread met values outside the fast range
+        for (int64_t b = gid; b < nv; b += stride)
+            for (int k = 0; k < V; ++k)
+                sq.add_slow(xv[b * V + k]);
+        if (gid < h + t)
+            sq.add_slow(x[scalar_index(gid, h, nv, V)]);
+    }
+    double s;
+    if (DOT) {
+        s = acc[0];
 #pragma unroll
-    for (int k = 1; k < V; ++k)
-        s += acc[k];
+        for (int k = 1; k < V; ++k)
+            s += acc[k];
+    } else {
+        s = sq.total();
+    }
     finish_reduction(s, o);
 }
 
@@ -277,10 +399,10 @@ __global__ void __launch_bounds__(kThreads)
     const double nalpha = -alpha;
     const int64_t gid = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    double acc[V];
-#pragma unroll
-    for (int k = 0; k < V; ++k)
-        acc[k] = 0.0;
+    SqAcc sq;
+    sq.init();
+    bool pending = false;
+    int chunk = 0;
     for (int64_t b = gid; b < nv; b += stride * UNROLL) {
         Vec<V> vp[UNROLL], va[UNROLL], vx[UNROLL], vr[UNROLL];
 #pragma unroll
@@ -301,11 +423,16 @@ __global__ void __launch_bounds__(kThreads)
                     vx[u].v[k] = __fma_rn(alpha, vp[u].v[k], vx[u].v[k]);
                     vr[u].v[k] = __fma_rn(nalpha, va[u].v[k], vr[u].v[k]);
                     if (RED)
-                        acc[k] = __fma_rn(vr[u].v[k], vr[u].v[k], acc[k]);
+                        sq.add(vr[u].v[k], pending);
                 }
                 st_stream<V>(x + e, vx[u]);
                 st_stream<V>(r + e, vr[u]);
             }
+        // flush the float-float chunk every 8 elements
+        if (RED && (chunk += UNROLL * V) >= 8) {
+            sq.flush();
+            chunk = 0;
+        }
     }
     if (gid < h + t) {
         const int64_t i = scalar_index(gid, h, nv, V);
@@ -313,14 +440,17 @@ __global__ void __launch_bounds__(kThreads)
         const double ri = __fma_rn(nalpha, Ap[i], r[i]);
         r[i] = ri;
         if (RED)
-            acc[0] = __fma_rn(ri, ri, acc[0]);
+            sq.add(ri, pending);
     }
     if (RED) {
-        double s = acc[0];
-#pragma unroll
-        for (int k = 1; k < V; ++k)
-            s += acc[k];
-        finish_reduction(s, o);
+        if (pending) {  // re-walk this thread's updated r for out-of-range values
+            for (int64_t b = gid; b < nv; b += stride)
+                for (int k = 0; k < V; ++k)
+                    sq.add_slow(r[h + b * V + k]);
+            if (gid < h + t)
+                sq.add_slow(r[scalar_index(gid, h, nv, V)]);
+        }
+        finish_reduction(sq.total(), o);
     }
 }
 

@@ -184,12 +184,17 @@ MESHES = [
 
 PLANNED = [
     (gen.CONFIGS["tiny"], None),
-    (gen.CONFIGS["tiny"], (100, 64, 200, 150)),
-    (gen.CONFIGS["tiny"], (7, 5, 9, 8)),
-    (gen.MeshConfig("masked", 6, 4, 17, 7), (500, 333, 700, 600)),
+    (gen.CONFIGS["tiny"], (100, 64, 200, 150, 1)),
+    (gen.CONFIGS["tiny"], (100, 64, 200, 150, 2)),
+    (gen.CONFIGS["tiny"], (100, 64, 200, 150, 4)),
+    (gen.CONFIGS["tiny"], (7, 5, 9, 8, 2)),
+    (gen.CONFIGS["tiny"], (7, 5, 9, 8, 4)),
+    (gen.MeshConfig("masked", 6, 4, 17, 7), (500, 333, 700, 600, 2)),
+    (gen.MeshConfig("masked4", 6, 4, 17, 7), (500, 333, 700, 600, 4)),
     (gen.MeshConfig("one", 1, 1, 5, 3), None),
-    (gen.MeshConfig("onemask", 1, 3, 5, 7), (3, 5, 7, 9)),
+    (gen.MeshConfig("onemask", 1, 3, 5, 7), (3, 5, 7, 9, 2)),
     (gen.CONFIGS["mid"], None),
+    (gen.CONFIGS["mid"], (24576, 24576, 24576, 22528, 2)),
     (gen.CONFIGS["large"], None),
 ]
 
@@ -234,7 +239,7 @@ def test_scatter_gather_unaligned_views(planned):
 def test_gather_sum_order_probe(planned):
     """Rows whose sum depends on order: 1.0 at the smallest local id, 2^-53 elsewhere."""
     cfg = gen.CONFIGS["tiny"]
-    m, t, ids = mesh_case(cfg, planned=planned, sizes=(50, 40, 60, 64) if planned else None)
+    m, t, ids = mesh_case(cfg, planned=planned, sizes=(50, 40, 60, 64, 2) if planned else None)
     tabs = m.tables()
     rs, li = tabs["rowStarts"], tabs["localIds"]
     for first in (True, False):
@@ -295,7 +300,7 @@ def test_out_of_range_entry_is_flagged_not_dereferenced():
 def test_bad_plan_entry_is_flagged_not_dereferenced():
     cfg = gen.CONFIGS["tiny"]
     m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
-    assert m.plan(100, 64, 200, 150) == bs.BS_OK
+    assert m.plan(100, 64, 200, 150, 2) == bs.BS_OK
     pt, pi = m.plan_tables(), m.plan_info()
     for key, bad in (("s_dst", 65535), ("s_src", 65535), ("g_src", 65535), ("g_pos", 65535)):
         corrupt = dict(pt)
@@ -358,3 +363,45 @@ def test_cg_iteration_sequence(name, planned):
     assert bits_equal(host(sc["rnorm"]), host(sc["rr_new"])) or rel_close(
         host(sc["rnorm"])[0], host(sc["rr_new"])[0])
     assert abs(alpha - ref["alpha"]) <= da
+
+
+def wide_range_vector(n, seed):
+    """Mantissas U(1,2) times 2^k, k in [-70, 70], random signs, with zeros and subnormals."""
+    m = 1.0 + (gen.uniform_pm1(seed, 1, n) + 1.0) / 2.0
+    k = np.floor((gen.uniform_pm1(seed, 2, n) + 1.0) * 70.5 - 70.0).astype(int)
+    x = np.ldexp(m, k) * np.sign(gen.uniform_pm1(seed, 3, n))
+    x[::97] = 0.0
+    x[5::211] = -0.0
+    x[7::503] = 5e-324 * np.arange(1, x[7::503].size + 1)
+    x[11::1009] = 2.0 ** 41      # exactly at the fast-range edge
+    x[13::1013] = 2.0 ** -40
+    return x
+
+
+@pytest.mark.parametrize("n", [1, 8, 1000, 1000003])
+def test_norm_wide_exponent_range(n):
+    x = wide_range_vector(n, 17)
+    got = host(bs.bs_norm(dev(x, 1)))[0]
+    assert rel_close(got, oracle.norm(x))
+    # each binade alone (sums dominated by one magnitude)
+    for k in (-45, -40, -39, 0, 40, 41, 60):
+        y = np.ldexp(1.0 + (gen.uniform_pm1(k + 100, 4, 4099) + 1.0) / 2.0, k)
+        assert rel_close(host(bs.bs_norm(dev(y)))[0], oracle.norm(y))
+
+
+def test_fused_residual_wide_exponent_range():
+    n = 300007
+    r = wide_range_vector(n, 23)
+    p, Ap, x = (gen.uniform_pm1(9, t, n) for t in (4, 5, 7))
+    pd, Apd, xd, rd = dev(p), dev(Ap), dev(x), dev(r)
+    rr = host(bs.bs_cg_update(pd, Apd, xd, rd, alpha=1e-30))[0]
+    xo, ro, rro = oracle.cg_update(1e-30, p, Ap, x, r)
+    assert bits_equal(host(rd), ro) and rel_close(rr, rro)
+
+
+def test_norm_non_finite():
+    x = gen.uniform_pm1(3, 3, 5000)
+    x[1234] = np.inf
+    assert host(bs.bs_norm(dev(x)))[0] == np.inf
+    x[17] = np.nan
+    assert np.isnan(host(bs.bs_norm(dev(x)))[0])

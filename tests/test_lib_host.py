@@ -135,7 +135,7 @@ def _seq_row_sums(vals, starts, lens):
 
 
 def simulate_plan_scatter(pt, pi, tabs, qG, NL):
-    T, B, BL = pi.s_ntiles, pi.s_nbuckets, pi.s_bucket_len
+    T, B, BL = pi.s_ntiles, pi.s_nbuckets, pi.s_bucket_len * pi.cluster
     rs, tr = tabs["rowStarts"], pt["s_tileRows"]
     run = pt["s_runStart"].reshape(T + 1, B)
     work = np.full(len(pt["s_src"]), np.nan)
@@ -154,8 +154,14 @@ def simulate_plan_scatter(pt, pi, tabs, qG, NL):
 
 
 def simulate_plan_gather(pt, pi, tabs, qL, NG):
-    U, C, TL = pi.g_ntiles, pi.g_nbuckets, pi.g_tile_len
-    rs, br, ts = tabs["rowStarts"], pt["g_bucketRows"], pt["g_tileSlot"]
+    U, C, TL, CS, MM = pi.g_ntiles, pi.g_nbuckets, pi.g_tile_len * pi.cluster, pi.cluster, pi.g_mmax
+    rs, ts = tabs["rowStarts"], pt["g_tileSlot"]
+    sub = pt["g_subRows"]
+    assert len(sub) == CS * C + 1 and np.all(np.diff(sub) >= 0)
+    sub_entries = rs[sub[1:]] - rs[sub[:-1]]
+    assert sub_entries.max() <= pi.g_bucket_entries and np.diff(sub).max() <= pi.g_bucket_entries
+    gs = pt["g_groupStart"].astype(np.int64).reshape(CS * C, MM + 1)
+    rowpos = pt["g_rowPos"].astype(np.int64)
     run = pt["g_runStart"].reshape(U + 1, C)
     work = np.full(len(pt["g_src"]), np.nan)
     for u in range(U):
@@ -166,17 +172,34 @@ def simulate_plan_gather(pt, pi, tabs, qL, NG):
         work[run[u][c] + (k - off[c])] = qL[u * TL:(u + 1) * TL][pt["g_src"][ts[u] + k]]
     qG = np.zeros(NG)
     for c in range(C):
-        r0, r1 = br[c], br[c + 1]
-        e0, e1 = rs[r0], rs[r1]
-        assert run[0, c] == e0 and run[U, c] == e1
-        vals = np.empty(e1 - e0)
-        vals[pt["g_pos"][e0:e1].astype(np.int64)] = work[e0:e1]
-        qG[r0:r1] = _seq_row_sums(vals, rs[r0:r1] - e0, np.diff(rs[r0:r1 + 1]))
+        E0, E1 = rs[sub[c * CS]], rs[sub[c * CS + CS]]
+        assert run[0, c] == E0 and run[U, c] == E1
+        vals = np.full(E1 - E0, np.nan)
+        vals[pt["g_pos"][E0:E1].astype(np.int64)] = work[E0:E1]
+        assert not np.any(np.isnan(vals))
+        for j in range(CS):
+            sb = c * CS + j
+            r0, r1 = sub[sb], sub[sb + 1]
+            lens = np.diff(rs[r0:r1 + 1])
+            assert gs[sb, 0] == 0 and gs[sb, MM] == lens.sum()
+            for m in range(1, MM + 1):
+                assert gs[sb, m] - gs[sb, m - 1] == m * int((lens == m).sum())
+                # rows of length m: consecutive m-slots in ascending row order
+                pos = rowpos[r0:r1][lens == m]
+                assert np.array_equal(pos, gs[sb, m - 1] + m * np.arange(len(pos)))
+            full = lens > 0
+            assert np.all(rowpos[r0:r1][~full] == 0xFFFF)
+            starts = rs[r0] - E0 + rowpos[r0:r1][full]
+            out = np.zeros(r1 - r0)
+            out[full] = _seq_row_sums(vals, starts, lens[full])
+            qG[r0:r1] = out
     return qG
 
 
-PLAN_CASES = [("tiny", None), ("tiny", (100, 64, 200, 150)), ("tiny", (7, 5, 9, 8)),
-              ("mid", None), ((5, 3, 7), (300, 256, 500, 333)), ((3, 4, 3), None)]
+PLAN_CASES = [("tiny", None), ("tiny", (100, 64, 200, 150, 1)), ("tiny", (100, 64, 200, 150, 2)),
+              ("tiny", (100, 64, 200, 150, 4)), ("tiny", (7, 5, 9, 8, 1)), ("tiny", (7, 5, 9, 8, 4)),
+              ("mid", None), ("mid", (24576, 24576, 24576, 22528, 2)),
+              ((5, 3, 7), (300, 256, 500, 333, 2)), ((3, 4, 3), None), ((2, 2, 7), (4, 3, 5, 8, 4))]
 
 
 @pytest.mark.parametrize("which,sizes", PLAN_CASES)
@@ -204,7 +227,11 @@ def test_two_pass_plan_reproduces_oracle(bs, which, sizes):
 
 def test_plan_rejects_bad_sizes_and_oversized_smem(bs):
     m = bs.Mesh(4, 3, 1)
-    assert m.plan(0, 10, 10, 10) == bs.BS_EINVAL and not m.plan_info().valid
-    assert m.plan(10, 70000, 10, 10) == bs.BS_EINVAL
-    assert m.plan(30000, 30000, 30000, 30000) == bs.BS_EINVAL    # > 227 KB of shared memory
-    assert m.plan(24576, 24576, 24576, 22528) == bs.BS_OK and m.plan_info().valid
+    pi = m.plan_info()
+    assert pi.valid and pi.cluster == 1 and pi.s_tile_rows == 24576
+    assert m.plan(0, 10, 10, 10, 1) == bs.BS_EINVAL and not m.plan_info().valid
+    assert m.plan(10, 70000, 10, 10, 1) == bs.BS_EINVAL
+    assert m.plan(30000, 30000, 30000, 30000, 1) == bs.BS_EINVAL   # > 227 KB of shared memory
+    assert m.plan(24576, 24576, 24576, 22528, 4) == bs.BS_EINVAL   # offsets beyond 16 bits
+    assert m.plan(100, 100, 100, 100, 3) == bs.BS_EINVAL           # cluster of 3
+    assert m.plan(24576, 24576, 24576, 22528, 2) == bs.BS_OK and m.plan_info().valid
