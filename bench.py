@@ -48,9 +48,21 @@ METRIC = "achieved HBM GB/s per BS1–BS7 kernel and fraction of measured GB300 
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SRC = {
-    "copy": "bs_vec.cu", "axpy": "bs_vec.cu", "norm": "bs_vec.cu", "dot": "bs_vec.cu",
-    "cg_update": "bs_vec.cu", "gather": "bs_gs.cu", "scatter": "bs_gs.cu",
+    "copy": ("bs_vec.cu",), "axpy": ("bs_vec.cu",), "norm": ("bs_vec.cu",), "dot": ("bs_vec.cu",),
+    "cg_update": ("bs_vec.cu",), "gather": ("bs_gs.cu", "bs_gs2.cu"),
+    "scatter": ("bs_gs.cu", "bs_gs2.cu"),
 }
+# Library kernels of one default (two-pass) step, in launch order, and the
+# operation each belongs to.
+STEP_KERNELS = [
+    ("copy_kernel", "copy"), ("axpy_kernel", "axpy"), ("dot_kernel", "norm"),
+    ("dot_kernel", "dot"), ("cg_kernel", "cg_update"), ("gather_tile_kernel", "gather"),
+    ("gather_bucket_kernel", "gather"), ("scatter_tile_kernel", "scatter"),
+    ("scatter_bucket_kernel", "scatter"), ("scatter_tile_kernel", "cg_iteration"),
+    ("scatter_bucket_kernel", "cg_iteration"), ("gather_tile_kernel", "cg_iteration"),
+    ("gather_bucket_kernel", "cg_iteration"), ("dot_kernel", "cg_iteration"),
+    ("cg_kernel", "cg_iteration"), ("dot_kernel", "cg_iteration"),
+]
 
 
 def parse_args(argv=None):
@@ -59,10 +71,12 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    ap.add_argument("--config", choices=sorted(gen.CONFIGS), default="stress")
+    ap.add_argument("--config", choices=sorted(gen.WORKLOADS), default="stress")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-sample", type=float, default=0.25,
+    ap.add_argument("--cpu-sample", type=float, default=1.0,
                     help="fraction of the step the oracle runs for cpu_baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="repeat the oracle sample until this much CPU time has passed")
     ap.add_argument("--ref-sample", type=float, default=1.0 / 32,
                     help="fraction of the step per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
@@ -71,6 +85,10 @@ def parse_args(argv=None):
     ap.add_argument("--probe", action="store_true")
     ap.add_argument("--no-plan", action="store_true",
                     help="one-pass gather/scatter kernels instead of the two-pass plan")
+    ap.add_argument("--traffic-from", metavar="CSV",
+                    help="write profiles/ncu_traffic.json from an ncu launch list (CSV with "
+                         "gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum) "
+                         "of a default two-pass step, then exit")
     ap.add_argument("--soak", type=float, default=1.5,
                     help="seconds of untimed steps before warm-up (clock sampling)")
     return ap.parse_args(argv)
@@ -91,9 +109,12 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def src_sha(name):
-    with open(os.path.join(ROOT, "order_fem_cg_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def src_sha(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "order_fem_cg_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def ncu_traffic(kernel, config):
@@ -361,7 +382,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    cfg = gen.CONFIGS[args.config]
+    cfg = gen.WORKLOADS[args.config]
     samp = OracleSample(cfg, args.ref_sample)
     for _ in range(args.warmup):
         samp.step()
@@ -422,7 +443,7 @@ def run_gpu(args):
     dist = init_dist(torch, world, local_rank)
     import order_fem_cg_gb300 as bs
 
-    cfg = gen.CONFIGS[args.config]
+    cfg = gen.WORKLOADS[args.config]
     wl = Workload(cfg, torch, bs, device, planned=not args.no_plan)
     stream = torch.cuda.Stream(device)
     peak, peak_src = measured_peak()
@@ -502,11 +523,16 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         samp = OracleSample(cfg, args.cpu_sample, host=wl.h)
+        reps = 0
         t0 = time.perf_counter()
-        samp.step()
-        dt = time.perf_counter() - t0
-        cpu = {"value": samp.bytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": samp.describe(), "seconds": dt}
+        while True:
+            samp.step()
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_seconds or reps >= 50:
+                break
+        cpu = {"value": samp.bytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"{reps} x " + samp.describe(), "seconds": dt}
 
     if rank == 0:
         line = {
@@ -609,8 +635,48 @@ def run_probe(args):
     return 0
 
 
+def traffic_from_csv(path, config):
+    """Per-operation DRAM bytes per call from an ncu launch list of bench steps."""
+    import csv
+    import io
+    import re
+    lines = open(path).read().splitlines()
+    head = next(i for i, l in enumerate(lines) if l.startswith('"ID"'))
+    launches = {}
+    for r in csv.DictReader(io.StringIO("\n".join(lines[head:]))):
+        m = re.search(r"<unnamed>::(\w+_kernel)", r["Kernel Name"])
+        if not m:
+            continue
+        rec = launches.setdefault(int(r["ID"]), {"kernel": m.group(1)})
+        rec[r["Metric Name"]] = float(r["Metric Value"].replace(",", ""))
+    seq = [launches[i] for i in sorted(launches)]
+    steps = [seq[i:i + len(STEP_KERNELS)] for i in range(0, len(seq), len(STEP_KERNELS))]
+    steps = [st for st in steps if len(st) == len(STEP_KERNELS) and
+             all(k["kernel"] == want for k, (want, _) in zip(st, STEP_KERNELS))]
+    if not steps:
+        raise SystemExit("no complete default step found in the launch list")
+    out = {}
+    for op in KERNEL_SRC:
+        per = []
+        for st in steps:
+            b = sum(k["dram__bytes_read.sum"] + k["dram__bytes_write.sum"]
+                    for k, (_, o) in zip(st, STEP_KERNELS) if o == op)
+            per.append(b)
+        out[op] = {"bytes_per_launch": sum(per) / len(per), "config": config,
+                   "src_sha256": src_sha(KERNEL_SRC[op]), "steps": len(per)}
+    doc = {"source": os.path.basename(path), "note": "dram__bytes_read.sum + "
+           "dram__bytes_write.sum per call of each operation (all of its kernels), averaged "
+           "over the captured steps", "kernels": out}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(doc, f, indent=1)
+    print(json.dumps(doc, indent=1))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.traffic_from:
+        return traffic_from_csv(args.traffic_from, args.config)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

@@ -171,7 +171,7 @@ class MeshConfig:
 
 # The benchmark workloads: four box meshes (tiny, mid, large, stress) and the
 # vector-length sweep 2^10 .. 2^27 for the five mesh-free operations.
-CONFIGS = {
+WORKLOADS = {
     "tiny": MeshConfig("tiny", 8, 3, SEED_BASE + 0),
     "mid": MeshConfig("mid", 20, 7, SEED_BASE + 1),
     "large": MeshConfig("large", 32, 7, SEED_BASE + 3),

@@ -518,6 +518,7 @@ int grid_for(const bs_ctx *ctx, int blocks_per_sm, int64_t work_items, int cap)
 
 constexpr int kStreamUnroll = 2;
 constexpr int kReduceUnroll = 2;
+constexpr int kNormUnroll = 4;  // the norm computes ~25 instructions per element
 constexpr int kCgUnroll = 1;
 
 template <int V>
@@ -540,7 +541,8 @@ template <int V, bool DOT>
 void launch_dot(int grid, cudaStream_t s, const double *x, const double *y, const Plan &pl,
                 const RedOut &o)
 {
-    dot_kernel<V, kReduceUnroll, DOT><<<grid, kThreads, 0, s>>>(x, y, pl.h, pl.nv, pl.t, o);
+    dot_kernel<V, DOT ? kReduceUnroll : kNormUnroll, DOT><<<grid, kThreads, 0, s>>>(
+        x, y, pl.h, pl.nv, pl.t, o);
 }
 
 template <int V>
@@ -639,7 +641,7 @@ static int dot_common(bs_ctx *ctx, const char *name, int64_t n, const double *x,
     }
     const void *ps[2] = {x, dot ? y : x};
     const Plan pl = make_plan(n, ctx->tune.vec_width, ps, 2);
-    const int grid = reduce_grid(ctx, pl, kReduceUnroll);
+    const int grid = reduce_grid(ctx, pl, dot ? kReduceUnroll : kNormUnroll);
     const RedOut o{ctx->partials, ctx->counter, out};
     if (dot) {
         switch (pl.V) {

@@ -32,7 +32,7 @@ def close(a, b, rtol=1e-12):
 
 @pytest.mark.parametrize("planned", [True, False])
 def test_stress_step_matches_oracle(planned):
-    cfg = gen.CONFIGS["stress"]
+    cfg = gen.WORKLOADS["stress"]
     torch.cuda.set_device(0)
     wl = bench.Workload(cfg, torch, bs, torch.device("cuda", 0), planned=planned)
     assert wl.planned == planned

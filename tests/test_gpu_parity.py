@@ -170,32 +170,32 @@ def mesh_case(cfg, seg=None, planned=False, sizes=None):
 
 
 MESHES = [
-    (gen.CONFIGS["tiny"], None),
-    (gen.CONFIGS["tiny"], 8),
-    (gen.CONFIGS["tiny"], 1000),
-    (gen.CONFIGS["tiny"], 4096),
+    (gen.WORKLOADS["tiny"], None),
+    (gen.WORKLOADS["tiny"], 8),
+    (gen.WORKLOADS["tiny"], 1000),
+    (gen.WORKLOADS["tiny"], 4096),
     (gen.MeshConfig("masked", 6, 4, 17, 7), None),
     (gen.MeshConfig("plain", 5, 2, 3, 0), 3000),
     (gen.MeshConfig("one", 1, 1, 5, 3), None),
     (gen.MeshConfig("onemask", 1, 3, 5, 7), 8),
-    (gen.CONFIGS["mid"], None),
+    (gen.WORKLOADS["mid"], None),
 ]
 
 
 PLANNED = [
-    (gen.CONFIGS["tiny"], None),
-    (gen.CONFIGS["tiny"], (100, 64, 200, 150, 1)),
-    (gen.CONFIGS["tiny"], (100, 64, 200, 150, 2)),
-    (gen.CONFIGS["tiny"], (100, 64, 200, 150, 4)),
-    (gen.CONFIGS["tiny"], (7, 5, 9, 8, 2)),
-    (gen.CONFIGS["tiny"], (7, 5, 9, 8, 4)),
+    (gen.WORKLOADS["tiny"], None),
+    (gen.WORKLOADS["tiny"], (100, 64, 200, 150, 1)),
+    (gen.WORKLOADS["tiny"], (100, 64, 200, 150, 2)),
+    (gen.WORKLOADS["tiny"], (100, 64, 200, 150, 4)),
+    (gen.WORKLOADS["tiny"], (7, 5, 9, 8, 2)),
+    (gen.WORKLOADS["tiny"], (7, 5, 9, 8, 4)),
     (gen.MeshConfig("masked", 6, 4, 17, 7), (500, 333, 700, 600, 2)),
     (gen.MeshConfig("masked4", 6, 4, 17, 7), (500, 333, 700, 600, 4)),
     (gen.MeshConfig("one", 1, 1, 5, 3), None),
     (gen.MeshConfig("onemask", 1, 3, 5, 7), (3, 5, 7, 9, 2)),
-    (gen.CONFIGS["mid"], None),
-    (gen.CONFIGS["mid"], (24576, 24576, 24576, 22528, 2)),
-    (gen.CONFIGS["large"], None),
+    (gen.WORKLOADS["mid"], None),
+    (gen.WORKLOADS["mid"], (24576, 24576, 24576, 22528, 2)),
+    (gen.WORKLOADS["large"], None),
 ]
 
 
@@ -223,7 +223,7 @@ def check_scatter_gather(cfg, m, t, ids):
 
 @pytest.mark.parametrize("planned", [False, True])
 def test_scatter_gather_unaligned_views(planned):
-    cfg = gen.CONFIGS["tiny"]
+    cfg = gen.WORKLOADS["tiny"]
     m, t, ids = mesh_case(cfg, planned=planned)
     qG = gen.uniform_pm1(1, 1, cfg.NG)
     qLd = dev(np.zeros(cfg.NL), 1)            # 8-byte aligned only
@@ -238,7 +238,7 @@ def test_scatter_gather_unaligned_views(planned):
 @pytest.mark.parametrize("planned", [False, True])
 def test_gather_sum_order_probe(planned):
     """Rows whose sum depends on order: 1.0 at the smallest local id, 2^-53 elsewhere."""
-    cfg = gen.CONFIGS["tiny"]
+    cfg = gen.WORKLOADS["tiny"]
     m, t, ids = mesh_case(cfg, planned=planned, sizes=(50, 40, 60, 64, 2) if planned else None)
     tabs = m.tables()
     rs, li = tabs["rowStarts"], tabs["localIds"]
@@ -253,7 +253,7 @@ def test_gather_sum_order_probe(planned):
 
 @pytest.mark.parametrize("planned", [False, True])
 def test_gather_of_ones_and_identities(planned):
-    cfg = gen.CONFIGS["mid"]
+    cfg = gen.WORKLOADS["mid"]
     m, t, ids = mesh_case(cfg, planned=planned)
     mult = dev(np.zeros(cfg.NG))
     bs.bs_gather(t, dev(np.ones(cfg.NL)), mult)
@@ -271,7 +271,7 @@ def test_gather_of_ones_and_identities(planned):
 
 
 def test_out_of_range_entry_is_flagged_not_dereferenced():
-    cfg = gen.CONFIGS["tiny"]
+    cfg = gen.WORKLOADS["tiny"]
     m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
     tabs = m.tables()
     bad_ids = tabs["scatterIds"].copy()
@@ -298,7 +298,7 @@ def test_out_of_range_entry_is_flagged_not_dereferenced():
 
 
 def test_bad_plan_entry_is_flagged_not_dereferenced():
-    cfg = gen.CONFIGS["tiny"]
+    cfg = gen.WORKLOADS["tiny"]
     m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
     assert m.plan(100, 64, 200, 150, 2) == bs.BS_OK
     pt, pi = m.plan_tables(), m.plan_info()
@@ -321,7 +321,7 @@ def test_invalid_arguments_rejected():
         bs.bs_copy(x, x[:9])
     with pytest.raises(bs.BSError):
         bs.bs_copy(x[0:6], x[4:10])            # partial overlap
-    cfg = gen.CONFIGS["tiny"]
+    cfg = gen.WORKLOADS["tiny"]
     m, t, ids = mesh_case(cfg)
     buf = torch.zeros(cfg.NL, dtype=torch.float64, device=DEV)
     with pytest.raises(bs.BSError):
@@ -336,7 +336,7 @@ def test_invalid_arguments_rejected():
 @pytest.mark.parametrize("name,planned", [("tiny", False), ("mid", False), ("tiny", True),
                                           ("mid", True)])
 def test_cg_iteration_sequence(name, planned):
-    cfg = gen.CONFIGS[name]
+    cfg = gen.WORKLOADS[name]
     m, t, ids = mesh_case(cfg, planned=planned)
     NG = cfg.NG
     pG = gen.uniform_pm1(cfg.seed, gen.TAG_P, NG)

@@ -68,7 +68,7 @@ CASES = [("tiny", None), ("mid", None), ((2, 2, 0), None), ((3, 4, 7), None), ((
 @pytest.mark.parametrize("which,seg", CASES)
 def test_mesh_builder_matches_oracle(bs, which, seg):
     if isinstance(which, str):
-        cfg = gen.CONFIGS[which]
+        cfg = gen.WORKLOADS[which]
     else:
         E, N, flags = which
         cfg = gen.MeshConfig("t", E, N, 0xABC + E, flags)
@@ -205,7 +205,7 @@ PLAN_CASES = [("tiny", None), ("tiny", (100, 64, 200, 150, 1)), ("tiny", (100, 6
 @pytest.mark.parametrize("which,sizes", PLAN_CASES)
 def test_two_pass_plan_reproduces_oracle(bs, which, sizes):
     if isinstance(which, str):
-        cfg = gen.CONFIGS[which]
+        cfg = gen.WORKLOADS[which]
     else:
         E, N, flags = which
         cfg = gen.MeshConfig("t", E, N, 0x51 + E, flags)

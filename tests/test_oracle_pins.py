@@ -147,7 +147,7 @@ def test_normal_moments():
 
 def test_mesh_sizes(golden):
     for name, E, N, NL, NG in golden("mesh_sizes.txt"):
-        cfg = gen.CONFIGS[name]
+        cfg = gen.WORKLOADS[name]
         assert (cfg.E, cfg.N) == (int(E), int(N))
         assert cfg.NL == int(NL) and cfg.NG == int(NG)
         assert cfg.NL == cfg.K * (cfg.N + 1) ** 3
@@ -181,7 +181,7 @@ def test_multiplicity_closed_form_golden(golden):
 
 @pytest.mark.parametrize("which", ["tiny", "mid", (2, 2), (5, 4), (1, 3)])
 def test_gather_of_ones_is_multiplicity(which):
-    cfg, ep, npm, ids = mesh(gen.CONFIGS[which] if isinstance(which, str) else which)
+    cfg, ep, npm, ids = mesh(gen.WORKLOADS[which] if isinstance(which, str) else which)
     m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
     vals, counts = np.unique(m, return_counts=True)
     hist = dict(zip(vals.astype(int).tolist(), counts.tolist()))
@@ -207,7 +207,7 @@ def test_dense_Z_brute_force_2x2x2():
 
 @pytest.mark.parametrize("which", ["tiny", (3, 3)])
 def test_gather_scatter_identities(which):
-    cfg, ep, npm, ids = mesh(gen.CONFIGS[which] if isinstance(which, str) else which)
+    cfg, ep, npm, ids = mesh(gen.WORKLOADS[which] if isinstance(which, str) else which)
     m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
     u = gen.integers_dyadic(cfg.seed, gen.TAG_U, cfg.NG)
     assert np.array_equal(oracle.gather(ids, oracle.scatter(ids, u), cfg.NG), m * u)

@@ -32,13 +32,13 @@ def test_fit_recovers_parameters():
 
 
 def test_byte_counts_of_the_workload_meshes():
-    st = gen.CONFIGS["stress"]
+    st = gen.WORKLOADS["stress"]
     NL, NG = st.NL, st.NG
     assert pm.bytes_scatter(NL, NG) == 944_086_536
     assert pm.bytes_gather(NL, NG, NL, 0) - 4 - 4 == 1_076_391_180
     assert pm.bytes_copy(NL) == 16 * 56_623_104
-    tiny = gen.CONFIGS["tiny"]
+    tiny = gen.WORKLOADS["tiny"]
     assert pm.bytes_scatter(tiny.NL, tiny.NG) == 518_216
-    lg = gen.CONFIGS["large"]
+    lg = gen.WORKLOADS["large"]
     seq = pm.bytes_cg_iteration(lg.NL, lg.NG, lg.NL, 0) - 4 - 4
     assert seq == 24 * lg.NL + 92 * lg.NG
