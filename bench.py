@@ -83,6 +83,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--probe", action="store_true")
+    ap.add_argument("--mass-operator", action="store_true",
+                    help="time y = Z^T diag(d) Z x (fused, GLL mass diagonal) against a "
+                         "separate scatter + gather on --config")
     ap.add_argument("--no-plan", action="store_true",
                     help="one-pass gather/scatter kernels instead of the two-pass plan")
     ap.add_argument("--traffic-from", metavar="CSV",
@@ -424,6 +427,19 @@ def workload_config(cfg, gpus, planned=None):
 
 # ------------------------------------------------------------ GPU leg
 
+def aggregate_ranks(dist, torch, elapsed_ms, units, steps, device=None):
+    """Whole-job timing over ranks: the slowest rank's time, and the bytes all
+    ranks processed per second (weak scaling: every rank runs its own mesh).
+    Returns (max elapsed ms, world size, GB/s)."""
+    world = 1
+    if dist is not None and dist.is_initialized():
+        world = dist.get_world_size()
+        t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    return elapsed_ms, world, units * world * steps / (elapsed_ms * 1e-3) / 1e9
+
+
 def init_dist(torch, world, local_rank):
     if world <= 1:
         return None
@@ -476,13 +492,9 @@ def run_gpu(args):
     stop.synchronize()
     barrier()
     clocks = sampler.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, world, value = aggregate_ranks(dist, torch, start.elapsed_time(stop),
+                                               wl.step_bytes, args.steps, device)
     ms_per_step = elapsed_ms / args.steps
-    value = wl.step_bytes * world * args.steps / (elapsed_ms * 1e-3) / 1e9
 
     per = {}
     for i, name in enumerate(wl.names):
@@ -608,6 +620,45 @@ def run_sweep(args):
     return 0
 
 
+def run_mass_operator(args):
+    import torch
+
+    import order_fem_cg_gb300 as bs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cfg = gen.WORKLOADS[args.config]
+    mesh = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    t = mesh.to_device(0)
+    x = torch.from_numpy(gen.uniform_pm1(cfg.seed, gen.TAG_X, cfg.NG)).to(dev)
+    d = torch.from_numpy(gen.mass_diagonal(cfg.E, cfg.N)).to(dev)
+    y = torch.empty(cfg.NG, dtype=torch.float64, device=dev)
+    qL = torch.empty(cfg.NL, dtype=torch.float64, device=dev)
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    fused = timed(lambda: bs.bs_apply_diag(t, x, d, y), args.steps)
+    separate = timed(lambda: (bs.bs_scatter(t, x, qL), bs.bs_gather(t, qL, y)), args.steps)
+    nbytes = 16 * cfg.NG + 12 * cfg.NL   # read x, d, ids; write y
+    peak, src = measured_peak()
+    print(json.dumps({"mode": "mass_operator", "workload": cfg.name, "op": "y = Z^T diag(d) Z x",
+                      "fused_ms": fused, "scatter_plus_gather_ms": separate,
+                      "algorithmic_bytes": nbytes, "fused_GB/s": nbytes / (fused * 1e-3) / 1e9,
+                      "fused_frac": nbytes / (fused * 1e-3) / 1e9 / peak, "peak_source": src,
+                      "steps": args.steps}), flush=True)
+    return 0
+
+
 def run_probe(args):
     import torch
 
@@ -683,6 +734,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.probe:
         return run_probe(args)
+    if args.mass_operator:
+        return run_mass_operator(args)
     return run_gpu(args)
 
 

@@ -198,6 +198,30 @@ def mesh_perms(cfg: MeshConfig):
     return ep, npm
 
 
+def gll_nodes_weights(N: int):
+    """Gauss-Lobatto-Legendre nodes and weights on [-1, 1] (degree N, N+1 points):
+    the end points and the roots of P_N'; w_i = 2 / (N (N+1) P_N(x_i)^2)."""
+    leg = np.polynomial.legendre.Legendre
+    if N == 1:
+        x = np.array([-1.0, 1.0])
+    else:
+        x = np.concatenate([[-1.0], np.sort(leg.basis(N).deriv().roots().real), [1.0]])
+    w = 2.0 / (N * (N + 1) * leg.basis(N)(x) ** 2)
+    return x, w
+
+
+def mass_diagonal(E: int, N: int) -> np.ndarray:
+    """Diagonal GLL mass matrix of every element of an E^3 box mesh of
+    [0,1]^3, degree N, in local order (i fastest): w_i w_j w_k (h/2)^3,
+    h = 1/E.  An input coefficient array for the diagonal local operator."""
+    _, w = gll_nodes_weights(N)
+    q = N + 1
+    n = np.arange(q ** 3)
+    i, j, k = n % q, (n // q) % q, n // (q * q)
+    elem = w[i] * w[j] * w[k] * (0.5 / E) ** 3
+    return np.tile(elem, E ** 3)
+
+
 def sweep_vectors(log2n: int):
     """(x, y, alpha) of the sweep point n = 2^log2n: N(0,1) data, alpha ~ U(0.1, 1)."""
     n = 1 << log2n

@@ -114,7 +114,7 @@ typedef struct {
     const uint16_t *g_pos;       /* [nnz]                           */
     const uint16_t *g_groupStart; /* [cluster*g_nbuckets*(g_mmax+1)] */
     const uint16_t *g_rowPos;    /* [NG]                            */
-    double *work;                /* [work_len >= nnz] scratch       */
+    double *work;                /* [work_len >= nnz] scratch (2 nnz for bs_apply_diag) */
     int64_t work_len;
 } bs_plan_dev;
 
@@ -272,6 +272,22 @@ int bs_gather(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double *qG, voi
 
 /* BS7 scatter: qL[l] = qG[scatterIds[l]], or +0.0 where scatterIds[l] < 0. */
 int bs_scatter(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, double *qL, void *stream);
+
+/* ---- global operator of a diagonal element-local operator ------------------
+ * "Portable high-order finite element kernels I", eqs. (6)-(7): the global
+ * operators are S_G = Z^T S_L Z and M_G = Z^T M_L Z with block-diagonal local
+ * operators.  For a diagonal M_L with entries dL[l] (a lumped or GLL mass
+ * matrix) this computes
+ *   yG = Z^T (dL .* (Z xG)),  yG[g] = sum over l in row g, ascending, of
+ *   (dL[l] * xG[g]) rounded, starting from +0.0 --
+ * bitwise equal to bs_scatter, an elementwise product, and bs_gather.
+ * Fused: scatter pass 1, then one kernel that places the scatter runs of a
+ * local range, scales them and emits the gather runs of the same range, then
+ * gather pass 2 -- q_L never reaches HBM.  Needs t->plan with cluster 1,
+ * s_bucket_len == g_tile_len (the default plan) and work_len >= 2 nnz.
+ * xG [NG], dL [NL], yG [NG] device; yG must not overlap xG or dL. */
+int bs_apply_diag(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const double *dL,
+                  double *yG, void *stream);
 
 /* ---- one CG iteration's streaming sequence --------------------------------
  * With the identity as the element-local operator (S_G = Z^T S_L Z of eqs.

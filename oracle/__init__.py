@@ -159,6 +159,15 @@ def box_scatter_ids(E, N, elem_perm, node_perm, mask_boundary=False):
     return ids
 
 
+def apply_diag(ids, dL, xG):
+    """y_G = Z^T (d_L .* (Z x_G)): the global operator of a diagonal local
+    operator ("Portable high-order finite element kernels I", eqs. (6)-(7)).
+    Scatter, one rounded product per local value, gather in ascending local
+    order."""
+    qL = scatter(ids, xG)
+    return gather(ids, _f64(dL) * qL, np.asarray(xG).size)
+
+
 def cg_sequence(ids, pG, xG, rG, rr):
     """One CG iteration's streaming sequence with the identity local operator.
 

@@ -44,6 +44,7 @@ EXPORTS = (
     "bs_mesh_build_box", "bs_mesh_build_box_ex", "bs_mesh_info", "bs_mesh_tables",
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
     "bs_probe_dfma", "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
+    "bs_apply_diag",
 )
 
 
@@ -118,6 +119,7 @@ def _declare(lib):
         "bs_gather": ([_vp, ctypes.POINTER(GSDev), _vp, _vp, _vp], _int),
         "bs_scatter": ([_vp, ctypes.POINTER(GSDev), _vp, _vp, _vp], _int),
         "bs_cg_iteration": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 10, _int),
+        "bs_apply_diag": ([_vp, ctypes.POINTER(GSDev), _vp, _vp, _vp, _vp], _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
         "bs_mesh_plan": ([_vp] + [ctypes.c_int32] * 5, _int),
@@ -433,14 +435,15 @@ class DeviceTables:
             if a.dtype == np.uint16:
                 a = a.view(np.int16)        # same bits; torch has no general uint16 kernels
             up[k] = torch.from_numpy(a).to(dev)
-        work = torch.empty(max(self.nnz, 1), dtype=torch.float64, device=dev)
+        # 2 nnz: bs_apply_diag needs a second work array
+        work = torch.empty(max(2 * self.nnz, 1), dtype=torch.float64, device=dev)
         ints = dict(cluster=pinfo.cluster, s_ntiles=pinfo.s_ntiles, s_nbuckets=pinfo.s_nbuckets,
                     s_tile_rows=pinfo.s_tile_rows, s_bucket_len=pinfo.s_bucket_len,
                     g_ntiles=pinfo.g_ntiles, g_nbuckets=pinfo.g_nbuckets,
                     g_tile_len=pinfo.g_tile_len, g_bucket_entries_max=pinfo.g_bucket_entries_max,
                     g_bucket_rows_max=pinfo.g_bucket_rows_max, g_mmax=pinfo.g_mmax)
         ps = PlanDev(**ints, **{k: (up[k].data_ptr() if up[k].numel() else 0) for k in PLAN_TABLES},
-                     work=work.data_ptr(), work_len=self.nnz)
+                     work=work.data_ptr(), work_len=2 * self.nnz)
         self.plan = dict(up, work=work, info=pinfo)
         self.plan_struct = ps
         self.struct.plan = ctypes.addressof(ps)
@@ -492,6 +495,15 @@ def bs_scatter(tables, qG, qL, stream=None, ctx=None):
     ctx.check(lib.bs_scatter(ctx.handle, ctypes.byref(tables.struct), _vec(qG, "qG", tables.NG),
                              _vec(qL, "qL", tables.NL), _stream(stream)), "bs_scatter")
     return qL
+
+
+def bs_apply_diag(tables, xG, dL, yG, stream=None, ctx=None):
+    """yG <- Z^T (dL .* (Z xG)): the global operator of a diagonal local operator (fused)."""
+    ctx = _ctx(ctx, xG)
+    ctx.check(lib.bs_apply_diag(ctx.handle, ctypes.byref(tables.struct), _vec(xG, "xG", tables.NG),
+                                _vec(dL, "dL", tables.NL), _vec(yG, "yG", tables.NG),
+                                _stream(stream)), "bs_apply_diag")
+    return yG
 
 
 def bs_cg_iteration(tables, pG, pL, ApG, xG, rG, rr, pAp, rr_new, rnorm, stream=None, ctx=None):

@@ -350,3 +350,26 @@ extern "C" int bs_cg_iteration(bs_ctx *ctx, const bs_gs_dev *t, const double *pG
         return st;
     return bs_norm(ctx, n, rG, rnorm_dev, stream);
 }
+
+extern "C" int bs_apply_diag(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const double *dL,
+                             double *yG, void *stream)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (int st = check_tables(ctx, "bs_apply_diag", t, true))
+        return st;
+    if (!t->plan)
+        return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: needs a two-pass plan");
+    if ((t->NG > 0 && (!xG || !yG)) || (t->NL > 0 && !dL))
+        return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: NULL vector");
+    if (bs_overlap(xG, 8 * t->NG, yG, 8 * t->NG) || bs_overlap(dL, 8 * t->NL, yG, 8 * t->NG))
+        return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: yG overlaps xG or dL");
+    if ((reinterpret_cast<uintptr_t>(xG) | reinterpret_cast<uintptr_t>(dL) |
+         reinterpret_cast<uintptr_t>(yG)) & 7u)
+        return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: vectors must be 8-byte aligned");
+    if (int st = bs_check_device(ctx))
+        return st;
+    if (t->NG == 0)
+        return BS_OK;
+    return bs_apply_diag_planned(ctx, t, xG, dL, yG, static_cast<cudaStream_t>(stream));
+}

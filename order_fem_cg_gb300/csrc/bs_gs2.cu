@@ -48,6 +48,7 @@ struct PlanArgs {
     const uint16_t *g_src, *g_pos, *g_groupStart, *g_rowPos;
     double *work;
     int *err;
+    int pf_mode, pf_ahead;  // L2 prefetch of sequential inputs (see prefetch_l2)
 };
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p)
@@ -112,6 +113,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar)
             return true;
     }
     return false;
+}
+
+// Asks the bulk-copy engine to bring [p, p + bytes) into L2 (no data to the
+// SM, no completion to wait for).  Only whole 16-byte units inside the
+// range are requested, so nothing outside it is touched.
+__device__ __forceinline__ void prefetch_l2(const void *p, int64_t bytes)
+{
+    uintptr_t a = reinterpret_cast<uintptr_t>(p), e = a + static_cast<uintptr_t>(bytes);
+    a = (a + 15u) & ~static_cast<uintptr_t>(15);
+    e &= ~static_cast<uintptr_t>(15);
+    while (a < e) {
+        const uint32_t n = static_cast<uint32_t>(e - a < 65536u ? e - a : 65536u);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
+        a += n;
+    }
+}
+
+// [lo, hi) clamped into [0, n]; false if empty.
+__device__ __forceinline__ bool clamp_range(int64_t &lo, int64_t &hi, int64_t n)
+{
+    lo = lo < 0 ? 0 : (lo > n ? n : lo);
+    hi = hi < lo ? lo : (hi > n ? n : hi);
+    return hi > lo;
 }
 
 // Writes [src, src + bytes) of shared memory to global memory by the
@@ -374,6 +398,59 @@ __device__ __forceinline__ void map_cluster(double *mine, double **all)
     }
 }
 
+// ------------------------------------------- L2 prefetch of a block's inputs
+// Thread 0 of a block asks for its own block's sequential inputs and, with
+// pf_mode 2, for those of the block one wave (pf_ahead blocks) later, which
+// will run on some SM soon: L2 then stages what shared memory has no room
+// for.  Ranges come from the tables, clamped into the arrays.
+__device__ void pf_scatter_tile(const PlanArgs &a, int t, const double *qG)
+{
+    const int64_t B = a.s_nbuckets;
+    int64_t r0 = a.s_tileRows[t], r1 = a.s_tileRows[t + 1];
+    if (clamp_range(r0, r1, a.NG)) {
+        prefetch_l2(qG + r0, 8 * (r1 - r0));
+        int64_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
+        if (clamp_range(e0, e1, a.nnz))
+            prefetch_l2(a.s_src + e0, 2 * (e1 - e0));
+    }
+    prefetch_l2(a.s_runStart + t * B, 8 * B);
+}
+
+__device__ void pf_scatter_bucket(const PlanArgs &a, int b, const double *ws)
+{
+    int64_t j0 = a.s_runStart[b];
+    int64_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + b];
+    if (clamp_range(j0, j1, a.nnz)) {
+        prefetch_l2(ws + j0, 8 * (j1 - j0));
+        prefetch_l2(a.s_dst + j0, 2 * (j1 - j0));
+    }
+}
+
+__device__ void pf_gather_tile(const PlanArgs &a, int u, const double *qL)
+{
+    const int64_t C = a.g_nbuckets;
+    int64_t l0 = static_cast<int64_t>(u) * a.g_tile_len, l1 = l0 + a.g_tile_len;
+    if (clamp_range(l0, l1, a.NL))
+        prefetch_l2(qL + l0, 8 * (l1 - l0));
+    int64_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
+    if (clamp_range(s0, s1, a.nnz))
+        prefetch_l2(a.g_src + s0, 2 * (s1 - s0));
+    prefetch_l2(a.g_runStart + u * C, 8 * C);
+}
+
+__device__ void pf_gather_bucket(const PlanArgs &a, int c, const double *wg)
+{
+    int64_t b0 = a.g_subRows[c], b1 = a.g_subRows[c + 1];
+    if (!clamp_range(b0, b1, a.NG))
+        return;
+    prefetch_l2(a.g_rowPos + b0, 2 * (b1 - b0));
+    int64_t e0 = a.rowStarts[b0], e1 = a.rowStarts[b1];
+    if (clamp_range(e0, e1, a.nnz)) {
+        prefetch_l2(wg + e0, 8 * (e1 - e0));
+        prefetch_l2(a.g_pos + e0, 2 * (e1 - e0));
+    }
+}
+
 // --------------------------------------------------------------- scatter
 // One cluster per tile of CS * s_tile_rows global rows; block r stages rows
 // [r * s_tile_rows, (r+1) * s_tile_rows) of it and emits 1/CS of the slots.
@@ -386,6 +463,11 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
     int32_t *runOff = runPos + a.s_nbuckets;
     const int r = cluster_rank<CS>();
     const int t = blockIdx.x / CS;
+    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
+        pf_scatter_tile(a, t, qG);
+        if (a.pf_mode > 1 && t + a.pf_ahead < a.s_ntiles)
+            pf_scatter_tile(a, t + a.pf_ahead, qG);
+    }
     const int32_t r0 = a.s_tileRows[t], r1 = a.s_tileRows[t + 1];
     const int32_t nrows = r1 - r0;
     bool ok = r0 >= 0 && nrows >= 0 && nrows <= CS * a.s_tile_rows && r1 <= a.NG;
@@ -433,6 +515,11 @@ __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, doubl
     double *out = reinterpret_cast<double *>(smem);
     const int r = cluster_rank<CS>();
     const int b = blockIdx.x / CS;
+    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
+        pf_scatter_bucket(a, b, a.work);
+        if (a.pf_mode > 1 && b + a.pf_ahead < a.s_nbuckets)
+            pf_scatter_bucket(a, b + a.pf_ahead, a.work);
+    }
     const int32_t per = a.s_bucket_len;
     const int64_t l0 = static_cast<int64_t>(b) * CS * per;
     const int64_t rest = a.NL - l0;
@@ -500,6 +587,11 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
     int32_t *runOff = runPos + a.g_nbuckets;
     const int r = cluster_rank<CS>();
     const int u = blockIdx.x / CS;
+    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
+        pf_gather_tile(a, u, qL);
+        if (a.pf_mode > 1 && u + a.pf_ahead < a.g_ntiles)
+            pf_gather_tile(a, u + a.pf_ahead, qL);
+    }
     const int32_t per = a.g_tile_len;
     const int64_t l0 = static_cast<int64_t>(u) * CS * per;
     const int64_t rest = a.NL - l0;
@@ -552,6 +644,11 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
     __shared__ int grp_bad;
     const int r = cluster_rank<CS>();
     const int c = blockIdx.x / CS;
+    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
+        pf_gather_bucket(a, c, a.work);
+        if (a.pf_mode > 1 && c + a.pf_ahead < a.g_nbuckets)
+            pf_gather_bucket(a, c + a.pf_ahead, a.work);
+    }
     const int MM = a.g_mmax;
     // entry offsets of the CS sub-buckets relative to the bucket start
     int32_t sub[CS + 1];
@@ -672,6 +769,94 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
         flag(a.err);
 }
 
+// ------------------------------------------- fused Z^T diag(d) Z (pass 2 + 1)
+// One block per local range [u TL, (u+1) TL), which is at once scatter
+// bucket u and gather tile u (the plan has s_bucket_len == g_tile_len and
+// one block per cluster).  It places scatter bucket u's runs (read from
+// `ws`) in shared memory -- that is q_L = Z x on the range, masked locals
+// +0.0 --, multiplies by d_L, and emits gather tile u's runs into `wg`
+// directly, so q_L never reaches HBM.
+__global__ void __launch_bounds__(kT, 1)
+    fused_diag_kernel(PlanArgs a, const double *__restrict__ ws, const double *__restrict__ dL,
+                      double *__restrict__ wg)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    double *vals = reinterpret_cast<double *>(smem);
+    int32_t *runPos = reinterpret_cast<int32_t *>(vals + a.g_tile_len);
+    int32_t *runOff = runPos + a.g_nbuckets;
+    const int u = blockIdx.x;
+    if (a.pf_mode && threadIdx.x == 0) {
+        for (int k = 0; k < (a.pf_mode > 1 ? 2 : 1); ++k) {
+            const int v = u + k * a.pf_ahead;
+            if (v >= a.g_ntiles)
+                break;
+            pf_scatter_bucket(a, v, ws);
+            int64_t d0 = static_cast<int64_t>(v) * a.g_tile_len, d1 = d0 + a.g_tile_len;
+            if (clamp_range(d0, d1, a.NL))
+                prefetch_l2(dL + d0, 8 * (d1 - d0));
+            int64_t s0 = a.g_tileSlot[v], s1 = a.g_tileSlot[v + 1];
+            if (clamp_range(s0, s1, a.nnz))
+                prefetch_l2(a.g_src + s0, 2 * (s1 - s0));
+            prefetch_l2(a.g_runStart + static_cast<int64_t>(v) * a.g_nbuckets, 8ll * a.g_nbuckets);
+        }
+    }
+    const int64_t l0 = static_cast<int64_t>(u) * a.g_tile_len;
+    const int32_t len = static_cast<int32_t>(a.NL - l0 < a.g_tile_len ? a.NL - l0 : a.g_tile_len);
+    const int32_t j0 = a.s_runStart[u];
+    const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + u];
+    const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
+    bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len && s0 >= 0 &&
+              s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
+    for (int32_t i = threadIdx.x; i < len; i += kT)
+        vals[i] = 0.0;
+    const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
+    __syncthreads();  // zeroed
+    bool bad = false;
+    if (ok) {
+        for (int32_t j = j0 + threadIdx.x; j < j1; j += kU * kT) {
+            uint16_t d[kU];
+            double v[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int32_t jj = j + q * kT;
+                d[q] = jj < j1 ? ld_u16(a.s_dst + jj) : 0;
+                v[q] = jj < j1 ? ld_seq(ws + jj) : 0.0;
+            }
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+                if (j + q * kT < j1) {
+                    if (d[q] < len)
+                        vals[d[q]] = v[q];
+                    else
+                        bad = true;
+                }
+        }
+    }
+    // (commit_runs begins with a barrier: the placements are complete after it)
+    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runPos, runOff) && ok &&
+         runOff[a.g_nbuckets] == s1 - s0;
+    if (ok) {
+        for (int32_t i0 = threadIdx.x; i0 < len; i0 += kU * kT) {
+            double w[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+                w[q] = i0 + q * kT < len ? ld_seq(dL + l0 + i0 + q * kT) : 0.0;
+#pragma unroll
+            for (int q = 0; q < kU; ++q)
+                if (i0 + q * kT < len)
+                    vals[i0 + q * kT] = __dmul_rn(w[q], vals[i0 + q * kT]);
+        }
+    }
+    __syncthreads();  // scaled tile ready
+    if (ok) {
+        double *tile[1] = {vals};
+        if (emit_runs<1>(runPos, runOff, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, tile, len, len, wg))
+            bad = true;
+    }
+    if (bad || (!ok && threadIdx.x == 0))
+        flag(a.err);
+}
+
 int64_t smem_s1(const bs_plan_dev *p) { return 8ll * p->s_tile_rows + 4ll * p->s_nbuckets + 4ll * (p->s_nbuckets + 1); }
 int64_t smem_s2(const bs_plan_dev *p) { return 8ll * p->s_bucket_len; }
 int64_t smem_g1(const bs_plan_dev *p) { return 8ll * p->g_tile_len + 4ll * p->g_nbuckets + 4ll * (p->g_nbuckets + 1); }
@@ -775,6 +960,8 @@ PlanArgs make_args(const bs_ctx *ctx, const bs_gs_dev *t)
     a.g_rowPos = p->g_rowPos;
     a.work = p->work;
     a.err = ctx->dev_err;
+    a.pf_mode = ctx->tune.l2_prefetch;
+    a.pf_ahead = ctx->sms;
     return a;
 }
 
@@ -828,4 +1015,32 @@ int bs_gather_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double 
     case 2: return gather_cs<2>(ctx, a, p, qL, qG, s);
     default: return gather_cs<4>(ctx, a, p, qL, qG, s);
     }
+}
+
+int bs_apply_diag_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const double *dL,
+                          double *yG, cudaStream_t s)
+{
+    if (int st = check_plan(ctx, "bs_apply_diag", t, dL, xG))
+        return st;
+    const bs_plan_dev *p = t->plan;
+    if (p->cluster != 1 || p->s_bucket_len != p->g_tile_len || p->s_nbuckets != p->g_ntiles)
+        return bs_set_error(ctx, BS_EINVAL,
+                            "bs_apply_diag: the plan needs cluster 1 and scatter buckets equal to "
+                            "gather tiles (s_bucket_len == g_tile_len)");
+    if (p->work_len < 2 * t->nnz)
+        return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: work buffer shorter than 2 nnz");
+    if (bs_overlap(p->work, 8 * p->work_len, dL, 8 * t->NL) ||
+        bs_overlap(p->work, 8 * p->work_len, yG, 8 * t->NG))
+        return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: work buffer overlaps dL or yG");
+    PlanArgs a = make_args(ctx, t);
+    double *ws = p->work, *wg = p->work + t->nnz;
+    if (int st = launch(ctx, "scatter_tile_kernel", scatter_tile_kernel<1>, 1, p->s_ntiles,
+                        smem_s1(p), s, a, xG))
+        return st;
+    if (int st = launch(ctx, "fused_diag_kernel", fused_diag_kernel, 1, p->g_ntiles, smem_g1(p), s,
+                        a, static_cast<const double *>(ws), dL, wg))
+        return st;
+    a.work = wg;
+    return launch(ctx, "gather_bucket_kernel", gather_bucket_kernel<1>, 1, p->g_nbuckets,
+                  smem_g2(p), s, a, yG);
 }

@@ -20,6 +20,8 @@ struct bs_tune {
     int reduce_blocks_per_sm;  // BS3-BS5 grid = SMs x this (capped by kMaxReduceBlocks)
     int scatter_blocks_per_sm; // BS7 grid = SMs x this
     int vec_width;             // widest vector in doubles: 4 (32 B), 2 (16 B) or 1
+    int l2_prefetch;           // two-pass kernels: 0 none (default: measured fastest),
+                               // 1 own inputs, 2 also the inputs of the block one wave ahead
 };
 
 struct bs_ctx {
@@ -62,6 +64,8 @@ int bs_scatter_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, double
                        cudaStream_t s);
 int bs_gather_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double *qG,
                       cudaStream_t s);
+int bs_apply_diag_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const double *dL,
+                          double *yG, cudaStream_t s);
 
 // Do the byte ranges [a, a+na) and [b, b+nb) overlap?
 inline bool bs_overlap(const void *a, int64_t na, const void *b, int64_t nb)

@@ -405,3 +405,40 @@ def test_norm_non_finite():
     assert host(bs.bs_norm(dev(x)))[0] == np.inf
     x[17] = np.nan
     assert np.isnan(host(bs.bs_norm(dev(x)))[0])
+
+
+# ------------------------------------------- diagonal local operator (fused)
+
+FUSED = [
+    (gen.WORKLOADS["tiny"], None),
+    (gen.WORKLOADS["tiny"], (100, 64, 64, 150, 1)),
+    (gen.WORKLOADS["tiny"], (7, 9, 9, 8, 1)),
+    (gen.MeshConfig("masked", 6, 4, 17, 7), (500, 333, 333, 600, 1)),
+    (gen.MeshConfig("one", 1, 1, 5, 3), None),
+    (gen.WORKLOADS["mid"], None),
+    (gen.WORKLOADS["large"], None),
+]
+
+
+@pytest.mark.parametrize("cfg,sizes", FUSED, ids=lambda v: getattr(v, "name", str(v)))
+def test_apply_diag(cfg, sizes):
+    m, t, ids = mesh_case(cfg, planned=True, sizes=sizes)
+    x = gen.uniform_pm1(cfg.seed, gen.TAG_X, cfg.NG)
+    for d in (gen.mass_diagonal(cfg.E, cfg.N), 1.0 + 0.5 * gen.uniform_pm1(cfg.seed, 21, cfg.NL),
+              np.ones(cfg.NL)):
+        yd = dev(np.full(cfg.NG, np.nan))
+        bs.bs_apply_diag(t, dev(x), dev(d), yd)
+        assert bits_equal(host(yd), oracle.apply_diag(ids, d, x))
+    assert bs.default_context().device_status() == bs.BS_OK
+
+
+def test_apply_diag_rejects_unfusable_plans():
+    cfg = gen.WORKLOADS["tiny"]
+    x, d = dev(np.ones(cfg.NG)), dev(np.ones(cfg.NL))
+    for sizes in ((100, 64, 128, 150, 1), (100, 64, 64, 150, 2)):
+        m, t, ids = mesh_case(cfg, planned=True, sizes=sizes)
+        with pytest.raises(bs.BSError):
+            bs.bs_apply_diag(t, x, d, dev(np.zeros(cfg.NG)))
+    m, t, ids = mesh_case(cfg, planned=False)
+    with pytest.raises(bs.BSError):
+        bs.bs_apply_diag(t, x, d, dev(np.zeros(cfg.NG)))

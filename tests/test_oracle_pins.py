@@ -422,3 +422,56 @@ def test_planted_axpy_mistake_is_caught():
     unfused = alpha * x + y          # two roundings instead of one fma
     assert not np.array_equal(unfused, np.array(exact))
     assert np.array_equal(oracle.axpy(alpha, x, 1.0, y), np.array(exact))
+
+
+# ----------------------------------------------------------------------------
+# Diagonal local operator (mass matrix) pins
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 7])
+def test_gll_quadrature_exact_to_degree_2N_minus_1(N):
+    """GLL quadrature integrates polynomials of degree <= 2N-1 exactly
+    ("GPU accelerated spectral finite elements on all-hex meshes")."""
+    x, w = gen.gll_nodes_weights(N)
+    assert abs(w.sum() - 2.0) < 1e-14
+    for k in range(2 * N):
+        exact = 0.0 if k % 2 else 2.0 / (k + 1)
+        assert abs(float(np.sum(w * x ** k)) - exact) < 1e-13
+    # and not beyond (degree 2N has a quadrature error)
+    assert abs(float(np.sum(w * x ** (2 * N))) - 2.0 / (2 * N + 1)) > 1e-6
+
+
+def _check_mass_operator(apply, cfg, ids):
+    d = gen.mass_diagonal(cfg.E, cfg.N)
+    one = apply(ids, d, np.ones(cfg.NG))
+    assert abs(math.fsum(one) - 1.0) < 1e-12          # total volume of [0,1]^3
+    if not (cfg.flags & gen.MASK_BOUNDARY):
+        assert np.all(one > 0)
+    x = gen.uniform_pm1(5, 1, cfg.NG)
+    y = gen.uniform_pm1(5, 2, cfg.NG)
+    xy = math.fsum(x * apply(ids, d, y))
+    yx = math.fsum(y * apply(ids, d, x))
+    assert abs(xy - yx) <= 1e-12 * math.fsum(np.abs(x) * apply(ids, d, np.abs(y)))
+
+
+@pytest.mark.parametrize("which", ["tiny", (3, 2), (2, 5)])
+def test_mass_operator_volume_and_symmetry(which):
+    cfg, ep, npm, ids = mesh(gen.WORKLOADS[which] if isinstance(which, str) else which)
+    _check_mass_operator(oracle.apply_diag, cfg, ids)
+    # with d = 1 the operator is gather(scatter(.)) = multiplicity * u
+    u = gen.integers_dyadic(3, 3, cfg.NG)
+    m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
+    assert np.array_equal(oracle.apply_diag(ids, np.ones(cfg.NL), u), m * u)
+
+
+def test_planted_mass_operator_mistakes_are_caught():
+    cfg, ep, npm, ids = mesh((3, 2))
+    mutants = [
+        lambda ids_, d, x: oracle.gather(ids_, oracle.scatter(ids_, x), cfg.NG),          # no d
+        lambda ids_, d, x: oracle.gather(ids_, d * d * oracle.scatter(ids_, x), cfg.NG),  # d twice
+        lambda ids_, d, x: oracle.gather(ids_, d * np.roll(oracle.scatter(ids_, x), 1),   # off by one
+                                         cfg.NG),
+    ]
+    for wrong in mutants:
+        with pytest.raises(AssertionError):
+            _check_mass_operator(wrong, cfg, ids)
