@@ -303,17 +303,59 @@ class Workload:
     def d2h_bytes(self):
         return sum(t.numel() * 8 for t in self.hout.values()) + 8 * len(self.sc)
 
-    def step_e2e(self, stream):
+    # inputs and outputs of every operation, for the pipelined end-to-end step
+    OP_IO = {
+        "copy": (("a",), ("b",)), "axpy": (("c", "d"), ("d",)), "norm": (("e",), ()),
+        "dot": (("f", "g"), ()), "cg_update": (("P", "AP", "X", "R"), ("X", "R")),
+        "gather": (("qL1",), ("qG1",)), "scatter": (("qG2",), ("qL2",)),
+        "cg_iteration": (("pG", "xG", "rG"), ("xG", "rG")),
+    }
+
+    def e2e_setup(self, compute_stream):
+        """Streams and events of the pipelined end-to-end step: each operation's
+        inputs go in on a copy-in stream, its kernels run on the compute stream
+        once they have landed, its outputs go out on a copy-out stream, so the
+        copies of one operation overlap the kernels of its neighbours."""
         torch = self.torch
-        with torch.cuda.stream(stream):
-            for k, t in self.hin.items():
-                self.v[k].copy_(t, non_blocking=True)
-            self.sc["rr"].copy_(self.hsc_in, non_blocking=True)
-            self.step(stream)
-            for k, t in self.hout.items():
-                t.copy_(self.v[k], non_blocking=True)
+        self.s_in = torch.cuda.Stream(self.device)
+        self.s_out = torch.cuda.Stream(self.device)
+        self.s_comp = compute_stream
+        mk = lambda: {n: torch.cuda.Event() for n in self.names}  # noqa: E731
+        self.ev_in, self.ev_done, self.ev_out = mk(), mk(), mk()
+        self.ev_scalars_out = torch.cuda.Event()
+        torch.cuda.synchronize()
+        for n in self.names:            # first step: nothing to wait for
+            self.ev_out[n].record(self.s_out)
+        self.ev_scalars_out.record(self.s_out)
+
+    def step_e2e(self):
+        torch = self.torch
+        # the reductions below overwrite the scalars the previous step reads back
+        self.s_comp.wait_event(self.ev_scalars_out)
+        for n in self.names:
+            ins, outs = self.OP_IO[n]
+            with torch.cuda.stream(self.s_in):
+                # the previous step's kernels and copy-out of this operation are done
+                self.s_in.wait_event(self.ev_out[n])
+                for k in ins:
+                    self.v[k].copy_(self.hin[k], non_blocking=True)
+                if n == "cg_iteration":
+                    self.s_in.wait_event(self.ev_scalars_out)
+                    self.sc["rr"].copy_(self.hsc_in, non_blocking=True)
+                self.ev_in[n].record(self.s_in)
+            self.s_comp.wait_event(self.ev_in[n])
+            self.op(n, self.s_comp)
+            self.ev_done[n].record(self.s_comp)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(self.ev_done[n])
+                for k in outs:
+                    self.hout[k].copy_(self.v[k], non_blocking=True)
+                self.ev_out[n].record(self.s_out)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_done[self.names[-1]])
             torch.cat([self.sc[k] for k in self.sc], out=self.sc_cat)
             self.hsc_out.copy_(self.sc_cat, non_blocking=True)
+            self.ev_scalars_out.record(self.s_out)
 
 
 def bs_perf():
@@ -514,23 +556,27 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         wl.pin_host()
+        wl.e2e_setup(stream)
         n_e = max(1, min(args.e2e_steps, args.steps))
-        wl.step_e2e(stream)
-        stream.synchronize()
+        wl.step_e2e()
+        torch.cuda.synchronize()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
-        e0.record(stream)
+        e0.record(wl.s_in)
         for _ in range(n_e):
-            wl.step_e2e(stream)
-        e1.record(stream)
+            wl.step_e2e()
+        wl.s_out.wait_event(wl.ev_done[wl.names[-1]])
+        e1.record(wl.s_out)
         e1.synchronize()
+        torch.cuda.synchronize()
         wall = time.perf_counter() - t0
         barrier()
         e_ms = e0.elapsed_time(e1)
         e2e = {"value": wl.step_bytes * world * n_e / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": wl.h2d_bytes, "d2h_bytes_per_step": wl.d2h_bytes,
-               "steps": n_e, "ms_per_step": e_ms / n_e, "host_wall_ms_per_step": wall * 1e3 / n_e}
+               "steps": n_e, "ms_per_step": e_ms / n_e, "host_wall_ms_per_step": wall * 1e3 / n_e,
+               "pipeline": "per operation: copy-in stream -> compute stream -> copy-out stream"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
