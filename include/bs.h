@@ -105,12 +105,12 @@ typedef struct {
     int32_t g_bucket_rows_max, g_mmax;
     const int32_t *s_tileRows;   /* [s_ntiles+1]                    */
     const int32_t *s_runStart;   /* [(s_ntiles+1) * s_nbuckets]     */
-    const uint16_t *s_src;       /* [nnz]                           */
+    const uint16_t *s_src;       /* [nnz] bit 15: first slot of a run */
     const uint16_t *s_dst;       /* [nnz]                           */
     const int32_t *g_subRows;    /* [cluster * g_nbuckets + 1]      */
     const int32_t *g_tileSlot;   /* [g_ntiles+1]                    */
     const int32_t *g_runStart;   /* [(g_ntiles+1) * g_nbuckets]     */
-    const uint16_t *g_src;       /* [nnz]                           */
+    const uint16_t *g_src;       /* [nnz] bit 15: first slot of a run */
     const uint16_t *g_pos;       /* [nnz]                           */
     const uint16_t *g_groupStart; /* [cluster*g_nbuckets*(g_mmax+1)] */
     const uint16_t *g_rowPos;    /* [NG]                            */
@@ -228,13 +228,16 @@ int bs_mesh_destroy(bs_mesh *mesh);
  *   Gather: tiles of consecutive locals write per-bucket runs, a bucket
  *   being `cluster` consecutive sub-buckets of rows with at most
  *   g_bucket_entries entries and rows each (pass 1); each bucket places its
- *   values in shared memory grouped by row length, sums every row in
- *   ascending local order and writes its rows of q_G in order (pass 2).
+ *   values in shared memory grouped by row length (each group an
+ *   entries x rows column-major block), sums every row in ascending local
+ *   order and writes its rows of q_G in order (pass 2).
  *   Rows may have at most 32 entries (box meshes: 8).
  * A tile or bucket is held by a cluster of `cluster` (1, 2 or 4) thread
  * blocks sharing their shared memory; the sizes are per block: a scatter
  * tile has cluster * s_tile_rows rows, and so on.  cluster * size must be
- * <= 65536 (entries: <= 65535, g_bucket_entries >= 8).  A plan whose
+ * <= 32768 for the tiles (s_tile_rows, g_tile_len: pass-1 offsets are 15
+ * bits, bit 15 marking the first slot of each run), <= 65536 for
+ * s_bucket_len and <= 65535 for g_bucket_entries (>= 8).  A plan whose
  * kernels would need more than 227 KB of shared memory per block is left
  * invalid (valid = 0); then use the one-pass kernels. */
 typedef struct {

@@ -184,20 +184,21 @@ __device__ __forceinline__ void stage(double *dst, const double *src, int n)
 
 // In-place exclusive scan of a[0..n); a[n] receives the total.  All
 // threads of the block call it; it ends with a barrier.
-__device__ void block_exclusive_scan(int32_t *a, int n)
+template <class T>
+__device__ void block_exclusive_scan(T *a, int n)
 {
-    __shared__ int32_t warp_tot[kT / 32];
+    __shared__ T warp_tot[kT / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per = (n + kT - 1) / kT;
     const int i0 = threadIdx.x * per;
-    int32_t local = 0;
+    T local = 0;
     for (int k = 0; k < per; ++k)
         if (i0 + k < n)
             local += a[i0 + k];
-    int32_t v = local;
+    T v = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+        const T y = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o)
             v += y;
     }
@@ -205,20 +206,20 @@ __device__ void block_exclusive_scan(int32_t *a, int n)
         warp_tot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        int32_t w = warp_tot[lane];
+        T w = warp_tot[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            const T y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o)
                 w += y;
         }
         warp_tot[lane] = w;
     }
     __syncthreads();
-    int32_t prefix = (v - local) + (warp > 0 ? warp_tot[warp - 1] : 0);
+    T prefix = (v - local) + (warp > 0 ? warp_tot[warp - 1] : T(0));
     for (int k = 0; k < per; ++k)
         if (i0 + k < n) {
-            const int32_t x = a[i0 + k];
+            const T x = a[i0 + k];
             a[i0 + k] = prefix;
             prefix += x;
         }
@@ -227,26 +228,34 @@ __device__ void block_exclusive_scan(int32_t *a, int n)
     __syncthreads();
 }
 
-// (+0.0 + v[0]) + v[1] + ... + v[n-1], n >= 1, in that order.  A sum
-// started from +0.0 is never -0.0 and otherwise equals the same sum started
-// from v[0], so the first addition is replaced by mapping -0.0 to +0.0
-// with integer operations (binary64 adds are scarce on this GPU).
-__device__ __forceinline__ double row_sum(const double *v, int n)
+// (+0.0 + v[0]) + v[stride] + ... + v[(n-1) stride], n >= 1, in that
+// order.  A sum started from +0.0 is never -0.0 and otherwise equals the
+// same sum started from v[0], so the first addition is replaced by mapping
+// -0.0 to +0.0 with integer operations (binary64 adds are scarce on this
+// GPU).
+__device__ __forceinline__ double row_sum(const double *v, int n, int stride)
 {
     double s = v[0];
     for (int j = 1; j < n; ++j)
-        s += v[j];
+        s += v[j * stride];
     const long long b = __double_as_longlong(s);
     return (b << 1) == 0 ? 0.0 : s;
 }
 
-// Largest c in [0, n) with off[c] <= k, for 0 <= k < off[n].
-__device__ __forceinline__ int find_run(const int32_t *off, int n, int32_t k)
+// A tile's run table in shared memory: runs[b] = (runOff[b] << 32) | ci[b]
+// with runOff the exclusive scan of the run lengths and ci that of "run b
+// is not empty" (runs[nb] holds both totals).
+__device__ __forceinline__ int32_t run_off(int64_t r) { return static_cast<int32_t>(r >> 32); }
+__device__ __forceinline__ int32_t run_ci(int64_t r) { return static_cast<int32_t>(r); }
+
+// Largest b in [0, n) with runOff[b] <= k, for 0 <= k < runOff[n]: the
+// (non-empty) run holding slot k.
+__device__ __forceinline__ int find_run(const int64_t *runs, int n, int32_t k)
 {
     int lo = 0, hi = n;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (off[mid] <= k)
+        if (run_off(runs[mid]) <= k)
             lo = mid;
         else
             hi = mid;
@@ -256,8 +265,9 @@ __device__ __forceinline__ int find_run(const int32_t *off, int n, int32_t k)
 
 // The (tile, bucket) run table row of tile `t`, fetched into registers
 // (issued before the tile staging so both are in flight together), then
-// committed to shared memory: runPos[b] = work position of run (t, b),
-// runOff = exclusive scan of the run lengths (runOff[nb] = total).
+// committed to shared memory as the packed scan `runs` (see run_off) and
+// runD[i] = work position of the i-th non-empty run minus its runOff, so
+// that slot k of that run goes to work[runD[i] + k].
 constexpr int kRunRegs = 4;  // run-table entries per thread held in registers
 
 struct RunFetch {
@@ -276,9 +286,14 @@ __device__ __forceinline__ RunFetch fetch_runs(const int32_t *runStart, int t, i
     return f;
 }
 
-// Returns false (uniformly) on a bad table.
+__device__ __forceinline__ bool run_ok(int32_t p0, int32_t p1, int64_t nnz)
+{
+    return p0 >= 0 && p1 >= p0 && p1 <= nnz;
+}
+
+// Returns false (uniformly) on a bad table; its runs are then all empty.
 __device__ bool commit_runs(const RunFetch &f, const int32_t *runStart, int t, int nb,
-                            int64_t nnz, int32_t *runPos, int32_t *runOff)
+                            int64_t nnz, int64_t *runs, int32_t *runD)
 {
     __shared__ int bad_runs;
     if (threadIdx.x == 0)
@@ -288,9 +303,9 @@ __device__ bool commit_runs(const RunFetch &f, const int32_t *runStart, int t, i
     for (int j = 0; j < kRunRegs; ++j) {
         const int b = threadIdx.x + j * kT;
         if (b < nb) {
-            const bool ok = f.p0[j] >= 0 && f.p1[j] >= f.p0[j] && f.p1[j] <= nnz;
-            runPos[b] = ok ? f.p0[j] : 0;
-            runOff[b] = ok ? f.p1[j] - f.p0[j] : 0;
+            const bool ok = run_ok(f.p0[j], f.p1[j], nnz);
+            const int64_t len = ok ? f.p1[j] - f.p0[j] : 0;
+            runs[b] = (len << 32) | (len > 0);
             if (!ok)
                 bad_runs = 1;
         }
@@ -298,14 +313,31 @@ __device__ bool commit_runs(const RunFetch &f, const int32_t *runStart, int t, i
     for (int b = threadIdx.x + kRunRegs * kT; b < nb; b += kT) {
         const int32_t p0 = runStart[static_cast<int64_t>(t) * nb + b];
         const int32_t p1 = runStart[static_cast<int64_t>(t + 1) * nb + b];
-        const bool ok = p0 >= 0 && p1 >= p0 && p1 <= nnz;
-        runPos[b] = ok ? p0 : 0;
-        runOff[b] = ok ? p1 - p0 : 0;
+        const bool ok = run_ok(p0, p1, nnz);
+        const int64_t len = ok ? p1 - p0 : 0;
+        runs[b] = (len << 32) | (len > 0);
         if (!ok)
             bad_runs = 1;
     }
     __syncthreads();
-    block_exclusive_scan(runOff, nb);
+    block_exclusive_scan(runs, nb);
+#pragma unroll
+    for (int j = 0; j < kRunRegs; ++j) {
+        const int b = threadIdx.x + j * kT;
+        if (b < nb && run_ok(f.p0[j], f.p1[j], nnz) && f.p1[j] > f.p0[j]) {
+            const int64_t r = runs[b];
+            runD[run_ci(r)] = f.p0[j] - run_off(r);
+        }
+    }
+    for (int b = threadIdx.x + kRunRegs * kT; b < nb; b += kT) {
+        const int32_t p0 = runStart[static_cast<int64_t>(t) * nb + b];
+        const int32_t p1 = runStart[static_cast<int64_t>(t + 1) * nb + b];
+        if (run_ok(p0, p1, nnz) && p1 > p0) {
+            const int64_t r = runs[b];
+            runD[run_ci(r)] = p0 - run_off(r);
+        }
+    }
+    __syncthreads();
     return bad_runs == 0;
 }
 
@@ -322,46 +354,81 @@ __device__ __forceinline__ double *pick(double *const *all, int i)
         return i < 2 ? (i ? all[1] : all[0]) : (i == 3 ? all[3] : all[2]);
 }
 
-// Writes the tile's slots [kbeg, kend) to the work array run by run: slot
-// k of run c goes to work[runPos[c] + k - runOff[c]], its value taken from
-// the cluster's staged tile at offset src[base + k] (block o / per holds
-// offsets [o*per, (o+1)*per)).  Each warp takes chunks of 32 kU consecutive
-// slots (lane i: slots i, i+32, ...), so the src loads and the work stores
-// of a warp instruction are contiguous; a lane finds its run by one binary
-// search per chunk and then walks forward.
+// Bit 15 of a pass-1 source offset marks the first slot of a run.
+constexpr uint32_t kRunStart = 0x8000u;
+
+// Writes the tile's slots [kbeg, kend) to the work array: slot k of the
+// i-th non-empty run goes to work[runD[i] + k], its value taken from the
+// cluster's staged tile at offset src[base + k] & 0x7fff (block o / per
+// holds offsets [o*per, (o+1)*per)).  Each warp takes one contiguous range
+// of slots, 32 (one per lane) at a time, so the src loads and the work
+// stores of a warp instruction are contiguous.  A lane's run is the number
+// of run starts up to its slot (one ballot and a population count over the
+// warp's 32 slots), counted from the run holding the warp's first slot
+// (one binary search); the next range's offsets are loaded while the
+// current range is written.  Every destination is checked against the
+// work array's length, so a corrupted table cannot write outside it.
 template <int CS>
-__device__ __forceinline__ bool emit_runs(const int32_t *runPos, const int32_t *runOff, int nb,
+__device__ __forceinline__ bool emit_runs(const int64_t *runs, const int32_t *runD, int nb,
                                           int32_t kbeg, int32_t kend, const uint16_t *src,
                                           int64_t base, double *const *tile, int per, int nvals,
-                                          double *work)
+                                          double *work, int64_t nwork)
 {
-    constexpr int kChunk = 32 * kU;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kT / 32;
+    const int64_t n = kend - kbeg;
+    const int32_t wb = kbeg + static_cast<int32_t>(n * warp / kWarps);
+    const int32_t we = kbeg + static_cast<int32_t>(n * (warp + 1) / kWarps);
+    if (wb >= we)
+        return false;
+    const uint32_t le_mask = (2u << lane) - 1u;  // lanes <= this lane
+    const int32_t nne = run_ci(runs[nb]);         // non-empty runs (>= 1 here)
+    // non-empty runs starting before slot wb, minus one
+    const int64_t rb = runs[find_run(runs, nb, wb)];
+    int32_t before = run_ci(rb) + (run_off(rb) < wb ? 1 : 0) - 1;
     bool bad = false;
-    for (int32_t c0 = kbeg + warp * kChunk; c0 < kend; c0 += (kT / 32) * kChunk) {
-        uint16_t o[kU];
+    uint16_t o[kU], on[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int32_t k = wb + 32 * u + lane;
+        o[u] = k < we ? ld_u16(src + base + k) : 0;
+    }
+    for (int32_t c0 = wb; c0 < we; c0 += 32 * kU) {
+        const int32_t c1 = c0 + 32 * kU;
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            const int32_t k = c0 + lane + 32 * u;
-            o[u] = k < kend ? ld_u16(src + base + k) : 0;
+            const int32_t k = c1 + 32 * u + lane;
+            on[u] = k < we ? ld_u16(src + base + k) : 0;
         }
-        int c = find_run(runOff, nb, c0 + lane < kend ? c0 + lane : kend - 1);
+        // straight-line over the chunk (no early exit), so that the loads
+        // of later groups overlap the stores of earlier ones; slots past
+        // `we` carry offset 0 (no run start) and store nothing
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
-            const int32_t k = c0 + lane + 32 * u;
-            if (k < kend) {
-                while (c + 1 < nb && runOff[c + 1] <= k)
-                    ++c;
+            const int32_t k = c0 + 32 * u + lane;
+            const uint32_t raw = o[u];
+            const uint32_t starts = __ballot_sync(0xffffffffu, raw & kRunStart);
+            const int32_t c = before + __popc(starts & le_mask);
+            before += __popc(starts);
+            if (k < we) {
+                const uint32_t off = raw & (kRunStart - 1u);
                 double v = 0.0;
-                if (o[u] < nvals) {
-                    const int owner = CS == 1 ? 0 : o[u] / per;
-                    v = pick<CS>(tile, owner)[o[u] - owner * per];
+                if (off < static_cast<uint32_t>(nvals)) {
+                    const int owner = CS == 1 ? 0 : off / per;
+                    v = pick<CS>(tile, owner)[off - owner * per];
                 } else {
                     bad = true;
                 }
-                work[runPos[c] + (k - runOff[c])] = v;
+                const int64_t d = static_cast<int64_t>(runD[min(max(c, 0), nne - 1)]) + k;
+                if (d >= 0 && d < nwork)
+                    work[d] = v;
+                else
+                    bad = true;
             }
         }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            o[u] = on[u];
     }
     return bad;
 }
@@ -459,8 +526,8 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
-    int32_t *runPos = reinterpret_cast<int32_t *>(vals + a.s_tile_rows);
-    int32_t *runOff = runPos + a.s_nbuckets;
+    int64_t *runs = reinterpret_cast<int64_t *>(vals + a.s_tile_rows);
+    int32_t *runD = reinterpret_cast<int32_t *>(runs + a.s_nbuckets + 1);
     const int r = cluster_rank<CS>();
     const int t = blockIdx.x / CS;
     if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
@@ -483,8 +550,8 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
     const RunFetch rf = fetch_runs(a.s_runStart, t, a.s_nbuckets);
     if (!bulk)
         stage(vals, qG + r0 + m0, m1 - m0);
-    ok = commit_runs(rf, a.s_runStart, t, a.s_nbuckets, a.nnz, runPos, runOff) && ok &&
-         runOff[a.s_nbuckets] == e1 - e0;
+    ok = commit_runs(rf, a.s_runStart, t, a.s_nbuckets, a.nnz, runs, runD) && ok &&
+         run_off(runs[a.s_nbuckets]) == e1 - e0;
     if (bulk && !mbar_wait(&bar)) {
         ok = false;
         mbar_wait(&bar);
@@ -496,8 +563,8 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
         const int32_t total = e1 - e0;
         const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
         const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
-        if (emit_runs<CS>(runPos, runOff, a.s_nbuckets, kb, ke, a.s_src, e0, tile, a.s_tile_rows,
-                          nrows, a.work))
+        if (emit_runs<CS>(runs, runD, a.s_nbuckets, kb, ke, a.s_src, e0, tile, a.s_tile_rows,
+                          nrows, a.work, a.nnz))
             flag(a.err);
     } else if (threadIdx.x == 0) {
         flag(a.err);
@@ -583,8 +650,8 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
-    int32_t *runPos = reinterpret_cast<int32_t *>(vals + a.g_tile_len);
-    int32_t *runOff = runPos + a.g_nbuckets;
+    int64_t *runs = reinterpret_cast<int64_t *>(vals + a.g_tile_len);
+    int32_t *runD = reinterpret_cast<int32_t *>(runs + a.g_nbuckets + 1);
     const int r = cluster_rank<CS>();
     const int u = blockIdx.x / CS;
     if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
@@ -607,8 +674,8 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
     const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
     if (!bulk)
         stage(vals, qL + l0 + m0, m1 - m0);
-    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runPos, runOff) && ok &&
-         runOff[a.g_nbuckets] == s1 - s0;
+    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
+         run_off(runs[a.g_nbuckets]) == s1 - s0;
     if (bulk && !mbar_wait(&bar)) {
         ok = false;
         mbar_wait(&bar);
@@ -620,8 +687,8 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
         const int32_t total = s1 - s0;
         const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
         const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
-        if (emit_runs<CS>(runPos, runOff, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per, len,
-                          a.work))
+        if (emit_runs<CS>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per, len,
+                          a.work, a.nnz))
             flag(a.err);
     } else if (threadIdx.x == 0) {
         flag(a.err);
@@ -640,7 +707,7 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
     int32_t *grp = reinterpret_cast<int32_t *>(vals + a.g_bucket_entries_max);  // [mmax+1]
-    __shared__ int32_t rowPre[kMaxRow + 1];
+    __shared__ int32_t grpRows[kMaxRow + 1];  // rows of each length
     __shared__ int grp_bad;
     const int r = cluster_rank<CS>();
     const int c = blockIdx.x / CS;
@@ -680,22 +747,20 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
     ok = ok && E0 >= 0 && E0 + ne <= a.nnz && j0 == E0 && j1 == E0 + ne && nrows >= 0 && r1 <= a.NG;
     if (ok && threadIdx.x <= MM)
         grp[threadIdx.x] = a.g_groupStart[sb * (MM + 1) + threadIdx.x];
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0)
         grp_bad = 0;
-        rowPre[0] = 0;
-    }
     double *dst[CS];
     map_cluster<CS>(vals, dst);
     cluster_barrier<CS>();  // all blocks resident; grp staged
     if (ok && threadIdx.x == 0) {
-        // rows of length m: (grp[m] - grp[m-1]) / m; rowPre[m] = rows of length <= m
+        // rows of length m: (grp[m] - grp[m-1]) / m
         int bad = grp[0] != 0 || grp[MM] != mine;
         int32_t acc = 0;
         for (int m = 1; m <= MM; ++m) {
             const int32_t len = grp[m] - grp[m - 1];
             bad |= len < 0 || len % m != 0;
+            grpRows[m] = len / m;
             acc += len / m;
-            rowPre[m] = acc;
         }
         bad |= acc > nrows;
         grp_bad = bad;
@@ -731,17 +796,15 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
                 }
         }
     }
-    cluster_barrier<CS>();  // every placement has landed; rowPre ready
+    cluster_barrier<CS>();  // every placement has landed; grpRows ready
     const bool go = ok && grp_bad == 0;
     if (go) {
-        // sums in the grouped layout, in place into each row's first slot
-        const int32_t R = rowPre[MM];
-        for (int32_t q = threadIdx.x; q < R; q += kT) {
-            int m = 1;
-            while (m < MM && rowPre[m] <= q)
-                ++m;
-            const int32_t base = grp[m - 1] + (q - rowPre[m - 1]) * m;
-            vals[base] = row_sum(vals + base, m);
+        // sums group by group, in place into each row's first slot; a group
+        // is column-major, so the lanes of a warp read consecutive words
+        for (int m = 1; m <= MM; ++m) {
+            const int32_t R = grpRows[m], base = grp[m - 1];
+            for (int32_t q = threadIdx.x; q < R; q += kT)
+                vals[base + q] = row_sum(vals + base + q, m, R);
         }
     }
     __syncthreads();
@@ -782,8 +845,8 @@ __global__ void __launch_bounds__(kT, 1)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *vals = reinterpret_cast<double *>(smem);
-    int32_t *runPos = reinterpret_cast<int32_t *>(vals + a.g_tile_len);
-    int32_t *runOff = runPos + a.g_nbuckets;
+    int64_t *runs = reinterpret_cast<int64_t *>(vals + a.g_tile_len);
+    int32_t *runD = reinterpret_cast<int32_t *>(runs + a.g_nbuckets + 1);
     const int u = blockIdx.x;
     if (a.pf_mode && threadIdx.x == 0) {
         for (int k = 0; k < (a.pf_mode > 1 ? 2 : 1); ++k) {
@@ -833,8 +896,8 @@ __global__ void __launch_bounds__(kT, 1)
         }
     }
     // (commit_runs begins with a barrier: the placements are complete after it)
-    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runPos, runOff) && ok &&
-         runOff[a.g_nbuckets] == s1 - s0;
+    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
+         run_off(runs[a.g_nbuckets]) == s1 - s0;
     if (ok) {
         for (int32_t i0 = threadIdx.x; i0 < len; i0 += kU * kT) {
             double w[kU];
@@ -850,16 +913,17 @@ __global__ void __launch_bounds__(kT, 1)
     __syncthreads();  // scaled tile ready
     if (ok) {
         double *tile[1] = {vals};
-        if (emit_runs<1>(runPos, runOff, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, tile, len, len, wg))
+        if (emit_runs<1>(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, tile, len, len, wg,
+                         a.nnz))
             bad = true;
     }
     if (bad || (!ok && threadIdx.x == 0))
         flag(a.err);
 }
 
-int64_t smem_s1(const bs_plan_dev *p) { return 8ll * p->s_tile_rows + 4ll * p->s_nbuckets + 4ll * (p->s_nbuckets + 1); }
+int64_t smem_s1(const bs_plan_dev *p) { return 8ll * p->s_tile_rows + 8ll * (p->s_nbuckets + 1) + 4ll * p->s_nbuckets; }
 int64_t smem_s2(const bs_plan_dev *p) { return 8ll * p->s_bucket_len; }
-int64_t smem_g1(const bs_plan_dev *p) { return 8ll * p->g_tile_len + 4ll * p->g_nbuckets + 4ll * (p->g_nbuckets + 1); }
+int64_t smem_g1(const bs_plan_dev *p) { return 8ll * p->g_tile_len + 8ll * (p->g_nbuckets + 1) + 4ll * p->g_nbuckets; }
 int64_t smem_g2(const bs_plan_dev *p) { return 8ll * p->g_bucket_entries_max + 4ll * (kMaxRow + 1); }
 
 constexpr int64_t kSmemMax = 232448;
@@ -903,9 +967,9 @@ int check_plan(bs_ctx *ctx, const char *name, const bs_gs_dev *t, const void *qL
         p->g_bucket_rows_max < 1)
         return bs_set_error(ctx, BS_EINVAL, "%s: bad plan sizes", name);
     const int64_t cs = p->cluster;
-    if (cs * p->s_tile_rows > 65536 || cs * p->s_bucket_len > 65536 ||
-        cs * p->g_tile_len > 65536 || cs * p->g_bucket_entries_max > 65535)
-        return bs_set_error(ctx, BS_EINVAL, "%s: plan offsets exceed 16 bits", name);
+    if (cs * p->s_tile_rows > 32768 || cs * p->s_bucket_len > 65536 ||
+        cs * p->g_tile_len > 32768 || cs * p->g_bucket_entries_max > 65535)
+        return bs_set_error(ctx, BS_EINVAL, "%s: plan offsets exceed their 15 or 16 bits", name);
     if (cs * p->s_nbuckets * p->s_bucket_len < t->NL || cs * p->g_ntiles * p->g_tile_len < t->NL ||
         cs * p->s_ntiles * p->s_tile_rows < t->NG)
         return bs_set_error(ctx, BS_EINVAL, "%s: plan does not cover the mesh", name);

@@ -24,11 +24,12 @@
 // a tile is cluster x the per-block size; runs grow with tile x bucket.
 // A gather bucket is `cluster` consecutive sub-buckets, each a row range
 // of at most g_bucket_entries entries and rows held by one block.  Inside a
-// sub-bucket the values are staged grouped by row length m (all rows with
-// m entries together, m values per row, rows and their values in ascending
-// order), so that a warp sums rows of equal length with all lanes busy --
-// a binary64 warp instruction holds the SM's FP64 pipe for ~20 cycles on
-// GB300 however many lanes are active.
+// sub-bucket the values are staged grouped by row length m: the R rows
+// with m entries form an m x R column-major block (entry j of the group's
+// q-th row at j R + q, rows in ascending order), so that a warp sums rows
+// of equal length with all lanes busy -- a binary64 warp instruction holds
+// the SM's FP64 pipe for ~20 cycles on GB300 however many lanes are
+// active -- and its lanes read consecutive shared-memory words.
 // Sizes below are per block.
 struct bs_plan {
     bool valid = false;
@@ -39,18 +40,21 @@ struct bs_plan {
     int32_t g_mmax = 0;                                       // longest row
     std::vector<int32_t> s_tileRows;   // [s_ntiles+1]  first row of each scatter tile
     std::vector<int32_t> s_runStart;   // [(s_ntiles+1) x s_nbuckets] work position of run (t, b)
-    std::vector<uint16_t> s_src;       // [nnz] tile-major: row offset within the tile
+    std::vector<uint16_t> s_src;       // [nnz] tile-major: row offset within the tile,
+                                       // | BS_PLAN_RUN_START on a run's first slot
     std::vector<uint16_t> s_dst;       // [nnz] work order: local offset within the bucket
     std::vector<int32_t> g_subRows;    // [cluster x g_nbuckets + 1] first row of each sub-bucket
     std::vector<int32_t> g_tileSlot;   // [g_ntiles+1]  unmasked locals before each tile
     std::vector<int32_t> g_runStart;   // [(g_ntiles+1) x g_nbuckets]
-    std::vector<uint16_t> g_src;       // [nnz] tile-major: local offset within the tile
+    std::vector<uint16_t> g_src;       // [nnz] tile-major: local offset within the tile,
+                                       // | BS_PLAN_RUN_START on a run's first slot
     std::vector<uint16_t> g_pos;       // [nnz] work order: staged position within the bucket
     std::vector<uint16_t> g_groupStart; // [cluster x g_nbuckets x (g_mmax+1)] per sub-bucket:
                                         // [m-1] = first position of the rows of length m,
                                         // [g_mmax] = entries of the sub-bucket
     std::vector<uint16_t> g_rowPos;    // [NG] staged position of a row's first value within
-                                       // its sub-bucket, 0xFFFF for a row without entries
+                                       // its sub-bucket (where its sum is left), 0xFFFF for a
+                                       // row without entries
 };
 
 struct bs_mesh {
@@ -79,6 +83,9 @@ int64_t bs_plan_smem_s1(const bs_plan &p);
 int64_t bs_plan_smem_s2(const bs_plan &p);
 int64_t bs_plan_smem_g1(const bs_plan &p);
 int64_t bs_plan_smem_g2(const bs_plan &p);
+// Marks the first slot of a run in s_src / g_src (tile offsets are < 2^15).
+constexpr uint32_t BS_PLAN_RUN_START = 0x8000u;
+
 // Longest row the grouped gather supports.
 constexpr int32_t BS_PLAN_MMAX = 32;
 

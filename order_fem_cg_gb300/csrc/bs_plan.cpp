@@ -9,9 +9,11 @@
 
 #include "bs_mesh_impl.h"
 
+// Pass 1 holds the tile, the packed run scan (8 bytes per bucket, plus the
+// totals) and the work offset of every run (4 bytes per bucket).
 int64_t bs_plan_smem_s1(const bs_plan &p)
 {
-    return 8ll * p.s_tile_rows + 4ll * p.s_nbuckets + 4ll * (p.s_nbuckets + 1);
+    return 8ll * p.s_tile_rows + 8ll * (p.s_nbuckets + 1) + 4ll * p.s_nbuckets;
 }
 
 int64_t bs_plan_smem_s2(const bs_plan &p)
@@ -21,7 +23,7 @@ int64_t bs_plan_smem_s2(const bs_plan &p)
 
 int64_t bs_plan_smem_g1(const bs_plan &p)
 {
-    return 8ll * p.g_tile_len + 4ll * p.g_nbuckets + 4ll * (p.g_nbuckets + 1);
+    return 8ll * p.g_tile_len + 8ll * (p.g_nbuckets + 1) + 4ll * p.g_nbuckets;
 }
 
 int64_t bs_plan_smem_g2(const bs_plan &p)
@@ -36,9 +38,10 @@ void bs_plan_build(bs_mesh *m, int32_t TRc, int32_t BLc, int32_t TLc, int32_t EB
     bs_plan &p = m->plan;
     if (CS != 1 && CS != 2 && CS != 4)
         return;
-    // offsets inside a tile or bucket (whole cluster) are stored as 16 bits
-    if (TRc < 1 || BLc < 1 || TLc < 1 || EBc < 8 || static_cast<int64_t>(TRc) * CS > 65536 ||
-        static_cast<int64_t>(BLc) * CS > 65536 || static_cast<int64_t>(TLc) * CS > 65536 ||
+    // offsets inside a bucket (whole cluster) are stored as 16 bits, those
+    // inside a tile as 15 bits (bit 15 marks the first slot of a run)
+    if (TRc < 1 || BLc < 1 || TLc < 1 || EBc < 8 || static_cast<int64_t>(TRc) * CS > 32768 ||
+        static_cast<int64_t>(BLc) * CS > 65536 || static_cast<int64_t>(TLc) * CS > 32768 ||
         static_cast<int64_t>(EBc) * CS > 65535)
         return;
     const int64_t NL = m->NL, NG = m->NG, nnz = m->nnz;
@@ -97,7 +100,8 @@ void bs_plan_build(bs_mesh *m, int32_t TRc, int32_t BLc, int32_t TLc, int32_t EB
                     const int32_t l = li[e];
                     const int64_t b = l / BL;
                     const int32_t k = cur[b]++;
-                    p.s_src[base + off[b] + k] = static_cast<uint16_t>(g - r0);
+                    p.s_src[base + off[b] + k] =
+                        static_cast<uint16_t>((g - r0) | (k == 0 ? BS_PLAN_RUN_START : 0));
                     p.s_dst[p.s_runStart[t * B + b] + k] = static_cast<uint16_t>(l - b * BL);
                 }
         }
@@ -142,7 +146,10 @@ void bs_plan_build(bs_mesh *m, int32_t TRc, int32_t BLc, int32_t TLc, int32_t EB
         m->plan = bs_plan();
         return;
     }
-    // rows grouped by length inside each sub-bucket
+    // rows grouped by length inside each sub-bucket; the R rows of length m
+    // of a group form an m x R column-major block: entry j of the group's
+    // row q sits at groupStart[m-1] + j R + q, so that consecutive threads
+    // summing consecutive rows read consecutive shared-memory words
     const int32_t MM = std::max<int32_t>(m->max_row, 1);
     if (MM > BS_PLAN_MMAX) {
         m->plan = bs_plan();
@@ -166,14 +173,13 @@ void bs_plan_build(bs_mesh *m, int32_t TRc, int32_t BLc, int32_t TLc, int32_t EB
         gs[MM] = static_cast<uint16_t>(acc);
         for (int32_t g = p.g_subRows[sb]; g < p.g_subRows[sb + 1]; ++g) {
             const int32_t len = rs[g + 1] - rs[g];
-            if (len > 0) {
-                p.g_rowPos[g] = static_cast<uint16_t>(next[len]);
-                next[len] += len;
-            }
+            if (len > 0)
+                p.g_rowPos[g] = static_cast<uint16_t>(next[len]++);
         }
     }
-    // staged position of CSR entry e (row g, k-th entry) within its bucket:
-    // offset of its sub-bucket in the bucket + grouped position of the row + k
+    // staged position of CSR entry e (row g of length m, k-th entry) within
+    // its bucket: offset of its sub-bucket in the bucket + position of the
+    // row in its group block + k times the group's row count
     std::vector<int32_t> epos(NL, -1);
     for (int64_t e = 0; e < nnz; ++e)
         epos[li[e]] = static_cast<int32_t>(e);
@@ -222,11 +228,15 @@ void bs_plan_build(bs_mesh *m, int32_t TRc, int32_t BLc, int32_t TLc, int32_t EB
                     continue;
                 const int64_t c = subOf[g] / CS;
                 const int32_t k = cur[c]++;
-                p.g_src[base + off[c] + k] = static_cast<uint16_t>(l - l0);
+                p.g_src[base + off[c] + k] =
+                    static_cast<uint16_t>((l - l0) | (k == 0 ? BS_PLAN_RUN_START : 0));
                 const int64_t sb = subOf[g];
                 const int64_t in_bucket = rs[p.g_subRows[sb]] - rs[p.g_subRows[c * CS]];
-                p.g_pos[p.g_runStart[u * C + c] + k] =
-                    static_cast<uint16_t>(in_bucket + p.g_rowPos[g] + (epos[l] - rs[g]));
+                const int32_t len = rs[g + 1] - rs[g];
+                const uint16_t *gs = p.g_groupStart.data() + sb * (MM + 1);
+                const int64_t R = (gs[len] - gs[len - 1]) / len;
+                p.g_pos[p.g_runStart[u * C + c] + k] = static_cast<uint16_t>(
+                    in_bucket + p.g_rowPos[g] + (epos[l] - rs[g]) * R);
             }
         }
     }

@@ -23,6 +23,10 @@ def build_lib():
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    # Test modules import the package at collection time, which maps
+    # libbs.so into this process: rebuild a stale library before that, or
+    # the whole session would run the previous build.
+    build_lib()
 
 
 def read_golden(name):

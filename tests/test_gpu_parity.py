@@ -194,7 +194,7 @@ PLANNED = [
     (gen.MeshConfig("one", 1, 1, 5, 3), None),
     (gen.MeshConfig("onemask", 1, 3, 5, 7), (3, 5, 7, 9, 2)),
     (gen.WORKLOADS["mid"], None),
-    (gen.WORKLOADS["mid"], (24576, 24576, 24576, 22528, 2)),
+    (gen.WORKLOADS["mid"], (16384, 24576, 16384, 22528, 2)),
     (gen.WORKLOADS["large"], None),
 ]
 

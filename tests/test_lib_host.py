@@ -125,12 +125,13 @@ def test_seeded_permutation_matches_generator(bs):
 
 # ------------------------------------------------- two-pass plan (host)
 
-def _seq_row_sums(vals, starts, lens):
-    """Row sums from +0.0 in ascending order (vectorised over rows)."""
+def _seq_row_sums(vals, starts, lens, strides):
+    """Row sums from +0.0 in ascending order (vectorised over rows); entry k
+    of a row sits at start + k * stride."""
     s = np.zeros(len(starts))
     for k in range(int(lens.max()) if len(lens) else 0):
         m = lens > k
-        s[m] = s[m] + vals[starts[m] + k]
+        s[m] = s[m] + vals[starts[m] + k * strides[m]]
     return s
 
 
@@ -145,7 +146,12 @@ def simulate_plan_scatter(pt, pi, tabs, qG, NL):
         assert off[-1] == rs[r1] - rs[r0]
         k = np.arange(off[-1])
         c = np.searchsorted(off, k, side="right") - 1
-        work[run[t][c] + (k - off[c])] = qG[r0:r1][pt["s_src"][rs[r0] + k]]
+        src = pt["s_src"][rs[r0] + k].astype(np.int64)
+        # bit 15 marks exactly the first slot of every non-empty run
+        first = np.zeros(off[-1], bool)
+        first[off[:-1][np.diff(off) > 0]] = True
+        assert np.array_equal(src >= 0x8000, first)
+        work[run[t][c] + (k - off[c])] = qG[r0:r1][src & 0x7FFF]
     qL = np.zeros(NL)
     for b in range(B):
         j0, j1 = run[0, b], run[T, b]
@@ -169,7 +175,11 @@ def simulate_plan_gather(pt, pi, tabs, qL, NG):
         assert off[-1] == ts[u + 1] - ts[u]
         k = np.arange(off[-1])
         c = np.searchsorted(off, k, side="right") - 1
-        work[run[u][c] + (k - off[c])] = qL[u * TL:(u + 1) * TL][pt["g_src"][ts[u] + k]]
+        src = pt["g_src"][ts[u] + k].astype(np.int64)
+        first = np.zeros(off[-1], bool)
+        first[off[:-1][np.diff(off) > 0]] = True
+        assert np.array_equal(src >= 0x8000, first)
+        work[run[u][c] + (k - off[c])] = qL[u * TL:(u + 1) * TL][src & 0x7FFF]
     qG = np.zeros(NG)
     for c in range(C):
         E0, E1 = rs[sub[c * CS]], rs[sub[c * CS + CS]]
@@ -183,22 +193,26 @@ def simulate_plan_gather(pt, pi, tabs, qL, NG):
             lens = np.diff(rs[r0:r1 + 1])
             assert gs[sb, 0] == 0 and gs[sb, MM] == lens.sum()
             for m in range(1, MM + 1):
-                assert gs[sb, m] - gs[sb, m - 1] == m * int((lens == m).sum())
-                # rows of length m: consecutive m-slots in ascending row order
+                nm = int((lens == m).sum())
+                assert gs[sb, m] - gs[sb, m - 1] == m * nm
+                # rows of length m: an m x nm column-major block, rows in
+                # ascending order, entry k of a row nm slots after entry k-1
                 pos = rowpos[r0:r1][lens == m]
-                assert np.array_equal(pos, gs[sb, m - 1] + m * np.arange(len(pos)))
+                assert np.array_equal(pos, gs[sb, m - 1] + np.arange(nm))
             full = lens > 0
             assert np.all(rowpos[r0:r1][~full] == 0xFFFF)
             starts = rs[r0] - E0 + rowpos[r0:r1][full]
+            lf = lens[full]
+            strides = (gs[sb, lf] - gs[sb, lf - 1]) // lf
             out = np.zeros(r1 - r0)
-            out[full] = _seq_row_sums(vals, starts, lens[full])
+            out[full] = _seq_row_sums(vals, starts, lf, strides)
             qG[r0:r1] = out
     return qG
 
 
 PLAN_CASES = [("tiny", None), ("tiny", (100, 64, 200, 150, 1)), ("tiny", (100, 64, 200, 150, 2)),
               ("tiny", (100, 64, 200, 150, 4)), ("tiny", (7, 5, 9, 8, 1)), ("tiny", (7, 5, 9, 8, 4)),
-              ("mid", None), ("mid", (24576, 24576, 24576, 22528, 2)),
+              ("mid", None), ("mid", (16384, 24576, 16384, 22528, 2)),
               ((5, 3, 7), (300, 256, 500, 333, 2)), ((3, 4, 3), None), ((2, 2, 7), (4, 3, 5, 8, 4))]
 
 
@@ -232,6 +246,8 @@ def test_plan_rejects_bad_sizes_and_oversized_smem(bs):
     assert m.plan(0, 10, 10, 10, 1) == bs.BS_EINVAL and not m.plan_info().valid
     assert m.plan(10, 70000, 10, 10, 1) == bs.BS_EINVAL
     assert m.plan(30000, 30000, 30000, 30000, 1) == bs.BS_EINVAL   # > 227 KB of shared memory
-    assert m.plan(24576, 24576, 24576, 22528, 4) == bs.BS_EINVAL   # offsets beyond 16 bits
+    assert m.plan(24576, 24576, 24576, 22528, 4) == bs.BS_EINVAL   # offsets beyond 15 / 16 bits
+    assert m.plan(16385, 100, 100, 100, 2) == bs.BS_EINVAL         # tile offsets beyond 15 bits
+    assert m.plan(100, 100, 16385, 100, 2) == bs.BS_EINVAL
     assert m.plan(100, 100, 100, 100, 3) == bs.BS_EINVAL           # cluster of 3
-    assert m.plan(24576, 24576, 24576, 22528, 2) == bs.BS_OK and m.plan_info().valid
+    assert m.plan(16384, 24576, 16384, 22528, 2) == bs.BS_OK and m.plan_info().valid
