@@ -65,6 +65,24 @@ __device__ __forceinline__ double ld_seq(const double *p)
     return v;
 }
 
+// Two consecutive values (16-byte aligned) and two consecutive 16-bit
+// entries (4-byte aligned), read once, not kept in L1.
+__device__ __forceinline__ double2 ld_pair(const double *p)
+{
+    double2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.f64 {%0, %1}, [%2];"
+                 : "=d"(v.x), "=d"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_u16x2(const uint16_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void flag(int *err)
 {
     atomicOr(err, BS_DEVERR_BOUNDS);
@@ -182,6 +200,67 @@ __device__ __forceinline__ void stage(double *dst, const double *src, int n)
     }
 }
 
+// Calls put(idx[j], val[j]) once for every j in [j0, j1), in no particular
+// order, from all threads of the block.  Where val + j and idx + j can both
+// be read two entries at a time (16-byte values, 4-byte index pairs), each
+// thread has kP pairs in flight -- twice the entries of the one-at-a-time
+// loop (kP = kU) for about the same registers, which is what a latency-
+// bound placement needs; otherwise entries are read one at a time.
+template <int kP, class F>
+__device__ __forceinline__ void stream_entries(const uint16_t *idx, const double *val, int32_t j0,
+                                               int32_t j1, F &&put)
+{
+    if (j0 >= j1)
+        return;
+    const uintptr_t av = reinterpret_cast<uintptr_t>(val + j0);
+    const uintptr_t ai = reinterpret_cast<uintptr_t>(idx + j0);
+    const bool paired = (av & 7u) == 0 && (ai & 1u) == 0 && ((av >> 3) & 1u) == ((ai >> 1) & 1u);
+    if (paired) {
+        int32_t j = j0;
+        if ((av >> 3) & 1u) {  // one entry first, so that val + j is 16-byte aligned
+            if (threadIdx.x == 0)
+                put(ld_u16(idx + j), ld_seq(val + j));
+            ++j;
+        }
+        const int32_t np = (j1 - j) >> 1;
+        const double *vp = val + j;
+        const uint16_t *ip = idx + j;
+        for (int32_t q = threadIdx.x; q < np; q += kP * kT) {
+            double2 v[kP];
+            uint32_t p[kP];
+#pragma unroll
+            for (int i = 0; i < kP; ++i) {
+                const int32_t qq = q + i * kT;
+                v[i] = qq < np ? ld_pair(vp + 2 * qq) : make_double2(0.0, 0.0);
+                p[i] = qq < np ? ld_u16x2(ip + 2 * qq) : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < kP; ++i)
+                if (q + i * kT < np) {
+                    put(p[i] & 0xffffu, v[i].x);
+                    put(p[i] >> 16, v[i].y);
+                }
+        }
+        if (((j1 - j) & 1) && threadIdx.x == 32)
+            put(ld_u16(idx + j1 - 1), ld_seq(val + j1 - 1));
+    } else {
+        for (int32_t j = j0 + threadIdx.x; j < j1; j += kU * kT) {
+            uint16_t d[kU];
+            double v[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int32_t jj = j + u * kT;
+                d[u] = jj < j1 ? ld_u16(idx + jj) : 0;
+                v[u] = jj < j1 ? ld_seq(val + jj) : 0.0;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+                if (j + u * kT < j1)
+                    put(d[u], v[u]);
+        }
+    }
+}
+
 // In-place exclusive scan of a[0..n); a[n] receives the total.  All
 // threads of the block call it; it ends with a barrier.
 template <class T>
@@ -228,18 +307,22 @@ __device__ void block_exclusive_scan(T *a, int n)
     __syncthreads();
 }
 
-// (+0.0 + v[0]) + v[stride] + ... + v[(n-1) stride], n >= 1, in that
-// order.  A sum started from +0.0 is never -0.0 and otherwise equals the
-// same sum started from v[0], so the first addition is replaced by mapping
-// -0.0 to +0.0 with integer operations (binary64 adds are scarce on this
-// GPU).
+// v[0] + v[stride] + ... + v[(n-1) stride], n >= 1, in that order.  The
+// row sum of the gather, (+0.0 + v[0]) + v[stride] + ..., is this value
+// with -0.0 mapped to +0.0 (plus_zero): a sum started from +0.0 is never
+// -0.0 and otherwise equals the same sum started from v[0], so the first
+// binary64 addition (scarce on this GPU) is replaced by integer work.
 __device__ __forceinline__ double row_sum(const double *v, int n, int stride)
 {
     double s = v[0];
     for (int j = 1; j < n; ++j)
         s += v[j * stride];
-    const long long b = __double_as_longlong(s);
-    return (b << 1) == 0 ? 0.0 : s;
+    return s;
+}
+
+__device__ __forceinline__ double plus_zero(double s)
+{
+    return (__double_as_longlong(s) << 1) == 0 ? 0.0 : s;
 }
 
 // A tile's run table in shared memory: runs[b] = (runOff[b] << 32) | ci[b]
@@ -535,18 +618,23 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
         if (a.pf_mode > 1 && t + a.pf_ahead < a.s_ntiles)
             pf_scatter_tile(a, t + a.pf_ahead, qG);
     }
-    const int32_t r0 = a.s_tileRows[t], r1 = a.s_tileRows[t + 1];
+    // The plan's tiles are the row ranges [t TR, (t+1) TR) clipped to N_G,
+    // so the staging starts without waiting for a table; s_tileRows and
+    // the CSR entry range are loaded meanwhile and checked before use.
+    const int64_t TR = static_cast<int64_t>(CS) * a.s_tile_rows;
+    const int32_t r0 = static_cast<int32_t>(min(t * TR, a.NG));
+    const int32_t r1 = static_cast<int32_t>(min((t + 1) * TR, a.NG));
     const int32_t nrows = r1 - r0;
-    bool ok = r0 >= 0 && nrows >= 0 && nrows <= CS * a.s_tile_rows && r1 <= a.NG;
-    const int32_t e0 = ok ? a.rowStarts[r0] : 0, e1 = ok ? a.rowStarts[r1] : 0;
-    ok = ok && e0 >= 0 && e1 >= e0 && e1 <= a.nnz;
+    const int32_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
+    bool ok = a.s_tileRows[t] == r0 && a.s_tileRows[t + 1] == r1;
     __shared__ uint64_t bar;
     if (threadIdx.x == 0)
         mbar_init(&bar);
     __syncthreads();
-    const int32_t m0 = ok ? min(r * a.s_tile_rows, nrows) : 0;
-    const int32_t m1 = ok ? min((r + 1) * a.s_tile_rows, nrows) : 0;
+    const int32_t m0 = min(r * a.s_tile_rows, nrows);
+    const int32_t m1 = min((r + 1) * a.s_tile_rows, nrows);
     const bool bulk = stage_start(vals, qG + r0 + m0, m1 - m0, &bar);
+    ok = ok && e0 >= 0 && e1 >= e0 && e1 <= a.nnz;
     const RunFetch rf = fetch_runs(a.s_runStart, t, a.s_nbuckets);
     if (!bulk)
         stage(vals, qG + r0 + m0, m1 - m0);
@@ -605,26 +693,14 @@ __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, doubl
         const int32_t n = j1 - j0;
         const int32_t jb = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * r / CS);
         const int32_t je = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * (r + 1) / CS);
-        for (int32_t j = jb + threadIdx.x; j < je; j += kU * kT) {
-            uint16_t d[kU];
-            double v[kU];
-#pragma unroll
-            for (int u = 0; u < kU; ++u) {
-                const int32_t jj = j + u * kT;
-                d[u] = jj < je ? ld_u16(a.s_dst + jj) : 0;
-                v[u] = jj < je ? ld_seq(a.work + jj) : 0.0;
+        stream_entries<CS == 1 ? kU : 6>(a.s_dst, a.work, jb, je, [&](uint32_t d, double v) {
+            if (d < static_cast<uint32_t>(len)) {
+                const int owner = CS == 1 ? 0 : d / per;
+                pick<CS>(dst, owner)[d - owner * per] = v;
+            } else {
+                bad = true;
             }
-#pragma unroll
-            for (int u = 0; u < kU; ++u)
-                if (j + u * kT < je) {
-                    if (d[u] < len) {
-                        const int owner = CS == 1 ? 0 : d[u] / per;
-                        pick<CS>(dst, owner)[d[u] - owner * per] = v[u];
-                    } else {
-                        bad = true;
-                    }
-                }
-        }
+        });
     }
     if constexpr (CS == 1)  // the placements are read next by the bulk-copy engine
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -717,19 +793,42 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
             pf_gather_bucket(a, c + a.pf_ahead, a.work);
     }
     const int MM = a.g_mmax;
+    const int64_t sb = static_cast<int64_t>(c) * CS + r;
+    // Independent loads first: the bucket's work range, this block's rows
+    // and its group table.
+    const int32_t j0 = a.g_runStart[c];
+    const int32_t j1 = a.g_runStart[static_cast<int64_t>(a.g_ntiles) * a.g_nbuckets + c];
+    const int32_t r0 = a.g_subRows[sb], r1 = a.g_subRows[sb + 1];
+    const int32_t nrows = r1 - r0;
+    bool ok = MM >= 1 && MM <= kMaxRow && r0 >= 0 && nrows >= 0 && r1 <= a.NG;
+    if (MM >= 1 && MM <= kMaxRow && threadIdx.x <= MM)
+        grp[threadIdx.x] = a.g_groupStart[sb * (MM + 1) + threadIdx.x];
     // entry offsets of the CS sub-buckets relative to the bucket start
     int32_t sub[CS + 1];
-    bool ok = MM >= 1 && MM <= kMaxRow;
-    const int32_t b0 = a.g_subRows[static_cast<int64_t>(c) * CS];
-    ok = ok && b0 >= 0 && b0 <= a.NG;
-    const int32_t E0 = ok ? a.rowStarts[b0] : 0;
+    int32_t E0;
+    bool csr_ok = true;  // the plan agrees with the CSR (checked late)
+    if constexpr (CS == 1) {
+        // the bucket's work range is its CSR entry range: no dependent load
+        // before the placement; rowStarts is compared after it
+        E0 = j0;
+        sub[0] = 0;
+        sub[1] = j1 - j0;
+        ok = ok && sub[1] <= a.g_bucket_entries_max;
+        const int32_t s0 = ok ? a.rowStarts[r0] : 0, s1 = ok ? a.rowStarts[r1] : 0;
+        csr_ok = s0 == j0 && s1 == j1;
+    } else {
+        const int32_t b0 = a.g_subRows[static_cast<int64_t>(c) * CS];
+        ok = ok && b0 >= 0 && b0 <= a.NG;
+        E0 = ok ? a.rowStarts[b0] : 0;
 #pragma unroll
-    for (int j = 0; j <= CS; ++j) {
-        const int32_t row = a.g_subRows[static_cast<int64_t>(c) * CS + j];
-        ok = ok && row >= b0 && row <= a.NG;
-        sub[j] = ok ? a.rowStarts[row] - E0 : 0;
-        if (j > 0)
-            ok = ok && sub[j] >= sub[j - 1] && sub[j] - sub[j - 1] <= a.g_bucket_entries_max;
+        for (int j = 0; j <= CS; ++j) {
+            const int32_t row = a.g_subRows[static_cast<int64_t>(c) * CS + j];
+            ok = ok && row >= b0 && row <= a.NG;
+            sub[j] = ok ? a.rowStarts[row] - E0 : 0;
+            if (j > 0)
+                ok = ok && sub[j] >= sub[j - 1] && sub[j] - sub[j - 1] <= a.g_bucket_entries_max;
+        }
+        ok = ok && j0 == E0 && j1 == E0 + sub[CS];
     }
     int32_t mine0 = sub[0], mine1 = sub[1];
 #pragma unroll
@@ -739,14 +838,7 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
             mine1 = sub[w + 1];
         }
     const int32_t ne = sub[CS], mine = mine1 - mine0;
-    const int64_t sb = static_cast<int64_t>(c) * CS + r;
-    const int32_t r0 = a.g_subRows[sb], r1 = a.g_subRows[sb + 1];
-    const int32_t nrows = r1 - r0;
-    const int32_t j0 = a.g_runStart[c];
-    const int32_t j1 = a.g_runStart[static_cast<int64_t>(a.g_ntiles) * a.g_nbuckets + c];
-    ok = ok && E0 >= 0 && E0 + ne <= a.nnz && j0 == E0 && j1 == E0 + ne && nrows >= 0 && r1 <= a.NG;
-    if (ok && threadIdx.x <= MM)
-        grp[threadIdx.x] = a.g_groupStart[sb * (MM + 1) + threadIdx.x];
+    ok = ok && E0 >= 0 && ne >= 0 && E0 + ne <= a.nnz;
     if (threadIdx.x == 0)
         grp_bad = 0;
     double *dst[CS];
@@ -769,39 +861,36 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
     if (ok) {
         const int32_t jb = static_cast<int32_t>(static_cast<int64_t>(ne) * r / CS);
         const int32_t je = static_cast<int32_t>(static_cast<int64_t>(ne) * (r + 1) / CS);
-        for (int32_t j = jb + threadIdx.x; j < je; j += kU * kT) {
-            uint16_t p[kU];
-            double v[kU];
+        stream_entries<CS == 1 ? kU : 6>(a.g_pos + E0, a.work + E0, jb, je, [&](uint32_t p, double v) {
+            if (p < static_cast<uint32_t>(ne)) {
+                int owner = 0;
+                int32_t base = sub[0];
 #pragma unroll
-            for (int q = 0; q < kU; ++q) {
-                const int32_t jj = j + q * kT;
-                p[q] = jj < je ? ld_u16(a.g_pos + E0 + jj) : 0;
-                v[q] = jj < je ? ld_seq(a.work + E0 + jj) : 0.0;
-            }
-#pragma unroll
-            for (int q = 0; q < kU; ++q)
-                if (j + q * kT < je) {
-                    if (p[q] < ne) {
-                        int owner = 0;
-                        int32_t base = sub[0];
-#pragma unroll
-                        for (int w = 1; w < CS; ++w) {
-                            owner += p[q] >= sub[w];
-                            base = p[q] >= sub[w] ? sub[w] : base;
-                        }
-                        pick<CS>(dst, owner)[p[q] - base] = v[q];
-                    } else {
-                        bad = true;
-                    }
+                for (int w = 1; w < CS; ++w) {
+                    owner += p >= static_cast<uint32_t>(sub[w]);
+                    base = p >= static_cast<uint32_t>(sub[w]) ? sub[w] : base;
                 }
-        }
+                pick<CS>(dst, owner)[p - base] = v;
+            } else {
+                bad = true;
+            }
+        });
+    }
+    // the first rows' staged positions, in flight during the row sums
+    constexpr int kRP = 16;
+    uint16_t rp[kRP];
+#pragma unroll
+    for (int q = 0; q < kRP; ++q) {
+        const int32_t k = threadIdx.x + q * kT;
+        rp[q] = ok && k < nrows ? ld_u16(a.g_rowPos + r0 + k) : 0;
     }
     cluster_barrier<CS>();  // every placement has landed; grpRows ready
-    const bool go = ok && grp_bad == 0;
+    const bool go = ok && grp_bad == 0 && csr_ok;
     if (go) {
         // sums group by group, in place into each row's first slot; a group
         // is column-major, so the lanes of a warp read consecutive words
-        for (int m = 1; m <= MM; ++m) {
+        // (a one-entry row is its own sum)
+        for (int m = 2; m <= MM; ++m) {
             const int32_t R = grpRows[m], base = grp[m - 1];
             for (int32_t q = threadIdx.x; q < R; q += kT)
                 vals[base + q] = row_sum(vals + base + q, m, R);
@@ -809,7 +898,22 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
     }
     __syncthreads();
     if (go) {
-        for (int32_t k0 = threadIdx.x; k0 < nrows; k0 += kU * kT) {
+        // q_G[row] = the row's sum, +0.0 for a row without entries (0xFFFF)
+#pragma unroll
+        for (int q = 0; q < kRP; ++q) {
+            const int32_t k = threadIdx.x + q * kT;
+            if (k < nrows) {
+                double v = 0.0;
+                if (rp[q] != 0xFFFF) {
+                    if (rp[q] < mine)
+                        v = plus_zero(vals[rp[q]]);
+                    else
+                        bad = true;
+                }
+                qG[r0 + k] = v;
+            }
+        }
+        for (int32_t k0 = kRP * kT + threadIdx.x; k0 < nrows; k0 += kU * kT) {
             uint16_t p[kU];
 #pragma unroll
             for (int q = 0; q < kU; ++q)
@@ -820,7 +924,7 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
                     double v = 0.0;
                     if (p[q] != 0xFFFF) {
                         if (p[q] < mine)
-                            v = vals[p[q]];
+                            v = plus_zero(vals[p[q]]);
                         else
                             bad = true;
                     }
@@ -876,24 +980,12 @@ __global__ void __launch_bounds__(kT, 1)
     __syncthreads();  // zeroed
     bool bad = false;
     if (ok) {
-        for (int32_t j = j0 + threadIdx.x; j < j1; j += kU * kT) {
-            uint16_t d[kU];
-            double v[kU];
-#pragma unroll
-            for (int q = 0; q < kU; ++q) {
-                const int32_t jj = j + q * kT;
-                d[q] = jj < j1 ? ld_u16(a.s_dst + jj) : 0;
-                v[q] = jj < j1 ? ld_seq(ws + jj) : 0.0;
-            }
-#pragma unroll
-            for (int q = 0; q < kU; ++q)
-                if (j + q * kT < j1) {
-                    if (d[q] < len)
-                        vals[d[q]] = v[q];
-                    else
-                        bad = true;
-                }
-        }
+        stream_entries<6>(a.s_dst, ws, j0, j1, [&](uint32_t d, double v) {
+            if (d < static_cast<uint32_t>(len))
+                vals[d] = v;
+            else
+                bad = true;
+        });
     }
     // (commit_runs begins with a barrier: the placements are complete after it)
     ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
