@@ -21,6 +21,10 @@ Other modes:
   --sweep            BS1-BS5 at n = 2^10 .. 2^27, host-timed launch->sync
                      as the pages time, with the T(B) = T0 + B/Wmax fit.
   --probe            binary64 FMA pipe throughput probe.
+  --mass-operator    y = Z^T diag(d) Z x, fused against scatter + gather.
+  --cg-solve         CG on Z^T diag(d) Z (GLL mass): time per iteration on
+                     --config, eager launches against one CUDA-graph replay,
+                     and the same on the tiny mesh, where launches dominate.
   --config NAME      another mesh workload (tiny, mid, large, stress).
 """
 
@@ -86,6 +90,9 @@ def parse_args(argv=None):
     ap.add_argument("--mass-operator", action="store_true",
                     help="time y = Z^T diag(d) Z x (fused, GLL mass diagonal) against a "
                          "separate scatter + gather on --config")
+    ap.add_argument("--cg-solve", action="store_true",
+                    help="time CG iterations on the GLL mass operator (eager and CUDA graph)")
+    ap.add_argument("--cg-iters", type=int, default=20)
     ap.add_argument("--no-plan", action="store_true",
                     help="one-pass gather/scatter kernels instead of the two-pass plan")
     ap.add_argument("--traffic-from", metavar="CSV",
@@ -705,6 +712,78 @@ def run_mass_operator(args):
     return 0
 
 
+def cg_solve_times(cfg, iters, reps, warmup, torch, bs, dev):
+    """(eager ms, graph ms) per CG iteration on cfg's mesh, mass operator:
+    a solve of `iters` iterations minus one of 0 iterations (the setup),
+    each timed with events over `reps` calls after `warmup` calls."""
+    mesh = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    t = mesh.to_device(0)
+    NG = cfg.NG
+    d = torch.from_numpy(gen.mass_diagonal(cfg.E, cfg.N)).to(dev)
+    b = torch.from_numpy(gen.uniform_pm1(cfg.seed, gen.TAG_R, NG)).to(dev)
+    x, r, p, Ap = (torch.zeros(NG, dtype=torch.float64, device=dev) for _ in range(4))
+    scal = {k: torch.zeros(2 * k + 1, dtype=torch.float64, device=dev) for k in (0, iters)}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+
+    def solve(k):
+        x.zero_()
+        bs.bs_cg_solve(t, d, b, x, r, p, Ap, k, scal[k], stream=s)
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                fn()
+            s.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            for _ in range(reps):
+                fn()
+            e1.record(s)
+            e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    eager = {k: timed(lambda k=k: solve(k)) for k in (0, iters)}
+    graphs = {}
+    for k in (0, iters):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            solve(k)
+        graphs[k] = g
+    graph = {k: timed(graphs[k].replay) for k in (0, iters)}
+    rr = scal[iters].cpu().numpy()[:iters + 1]
+    return ((eager[iters] - eager[0]) / iters, (graph[iters] - graph[0]) / iters,
+            float(rr[-1] / rr[0]))
+
+
+def run_cg_solve(args):
+    import torch
+
+    import order_fem_cg_gb300 as bs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cfg = gen.WORKLOADS[args.config]
+    K = max(1, args.cg_iters)
+    reps = max(3, min(args.steps, 20))
+    eager, graph, rr_ratio = cg_solve_times(cfg, K, reps, max(3, args.warmup), torch, bs, dev)
+    # per iteration: y = A p (x, y, d, one index per local), p.Ap, BS5, p update
+    nbytes = 16 * cfg.NG + 12 * cfg.NL + 16 * cfg.NG + 48 * cfg.NG + 24 * cfg.NG
+    peak, src = measured_peak()
+    tiny = gen.WORKLOADS["tiny"]
+    t_eager, t_graph, _ = cg_solve_times(tiny, 50, 20, 3, torch, bs, dev)
+    print(json.dumps({
+        "mode": "cg_solve", "workload": cfg.name, "operator": "A = Z^T diag(GLL mass) Z",
+        "iters": K, "rr_ratio": rr_ratio, "launches_per_iter": 6,
+        "eager_ms_per_iter": eager, "graph_ms_per_iter": graph,
+        "bytes_per_iter": nbytes, "GB/s": nbytes / (graph * 1e-3) / 1e9,
+        "frac": nbytes / (graph * 1e-3) / 1e9 / peak, "peak_source": src,
+        "tiny": {"workload": tiny.name, "eager_us_per_iter": 1e3 * t_eager,
+                 "graph_us_per_iter": 1e3 * t_graph,
+                 "launch_us_saved_per_kernel": 1e3 * (t_eager - t_graph) / 6}}), flush=True)
+    return 0
+
+
 def run_probe(args):
     import torch
 
@@ -782,6 +861,8 @@ def main(argv=None):
         return run_probe(args)
     if args.mass_operator:
         return run_mass_operator(args)
+    if args.cg_solve:
+        return run_cg_solve(args)
     return run_gpu(args)
 
 

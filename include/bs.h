@@ -165,6 +165,14 @@ int bs_copy(bs_ctx *ctx, int64_t n, const double *x, double *y, void *stream);
 int bs_axpy(bs_ctx *ctx, int64_t n, double alpha, const double *x, double beta, double *y,
             void *stream);
 
+/* BS2 with beta formed on the device: beta = *beta_num_dev / *beta_den_dev
+ * (0 where the denominator is 0), then as bs_axpy.  CG's direction update
+ * p = r + beta p with beta = rr_new / rr (alpha = 1) without a host round
+ * trip.  The scalars must not lie inside y. */
+int bs_axpy_dev(bs_ctx *ctx, int64_t n, double alpha, const double *x,
+                const double *beta_num_dev, const double *beta_den_dev, double *y,
+                void *stream);
+
 /* BS3 norm: *out_dev = sum_i x[i]^2 -- the squared 2-norm, "norm:
  * alpha = x.x"; take the square root yourself. */
 int bs_norm(bs_ctx *ctx, int64_t n, const double *x, double *out_dev, void *stream);
@@ -178,7 +186,8 @@ int bs_dot(bs_ctx *ctx, int64_t n, const double *x, const double *y, double *out
  *   *rdotr_dev = sum_i r[i]^2 over the updated r.
  * alpha is `alpha` unless both alpha_num_dev and alpha_den_dev are given,
  * in which case alpha = *alpha_num_dev / *alpha_den_dev is formed on the
- * device (CG's alpha = (r.r) / (p.Ap) without a host round trip).
+ * device (CG's alpha = (r.r) / (p.Ap) without a host round trip); a zero
+ * denominator gives alpha = 0 (p = 0 only at an exact solution).
  * rdotr_dev may be NULL (no reduction).  x and r must not overlap each
  * other or p, Ap. */
 int bs_cg_update(bs_ctx *ctx, int64_t n, const double *alpha_num_dev,
@@ -288,7 +297,9 @@ int bs_scatter(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, double *qL, vo
  * local range, scales them and emits the gather runs of the same range, then
  * gather pass 2 -- q_L never reaches HBM.  Needs t->plan with cluster 1,
  * s_bucket_len == g_tile_len (the default plan) and work_len >= 2 nnz.
- * xG [NG], dL [NL], yG [NG] device; yG must not overlap xG or dL. */
+ * xG [NG], dL [NL], yG [NG] device; yG must not overlap xG or dL.
+ * dL == NULL is the identity local operator: yG = Z^T Z xG (each global
+ * value times its number of local copies, summed as the gather sums). */
 int bs_apply_diag(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const double *dL,
                   double *yG, void *stream);
 
@@ -302,6 +313,31 @@ int bs_apply_diag(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const doubl
 int bs_cg_iteration(bs_ctx *ctx, const bs_gs_dev *t, const double *pG, double *pL, double *ApG,
                     double *xG, double *rG, const double *rr_dev, double *pAp_dev,
                     double *rr_new_dev, double *rnorm_dev, void *stream);
+
+/* ---- conjugate gradients on the global operator --------------------------
+ * "Portable high-order finite element kernels I": every benchmark problem
+ * solves its system by CG (its Algorithm 1, whose vector operations are
+ * y = alpha x + beta y, dot, norm and y = A x, with steps 8-10 fusable into
+ * BS5).  The algorithm's listing did not survive; this is the textbook
+ * (Hestenes-Stiefel) iteration those operations and that fusion describe,
+ * on A = Z^T diag(dL) Z (bs_apply_diag; dL == NULL: A = Z^T Z):
+ *   ApG = A xG;  rG = bG - ApG  (copy, then BS2 with alpha = -1);
+ *   pG = rG;  rr_0 = rG.rG (BS3)
+ *   for k = 0 .. iters-1:
+ *     ApG = A pG;  pAp_k = pG.ApG (BS4);  alpha = rr_k / pAp_k;
+ *     xG += alpha pG, rG -= alpha ApG, rr_{k+1} = rG.rG (BS5);
+ *     pG = rG + (rr_{k+1} / rr_k) pG (bs_axpy_dev)
+ * A zero denominator makes its quotient 0 (exact convergence keeps x).
+ * Every scalar stays on the device: scal_dev [2 iters + 1] receives
+ * rr_0 .. rr_iters, then pAp_0 .. pAp_{iters-1}.  xG holds x_0 on entry
+ * and x_iters on return; rG, pG, ApG [NG] are caller scratch (r_iters and
+ * p_iters on return).  Needs a plan as bs_apply_diag does.  Launches
+ * 3 + 4 + 6 iters kernels on `stream` and never synchronises, so the whole
+ * solve can be captured in a CUDA graph.  No convergence test: the caller
+ * reads rr_k when it chooses. */
+int bs_cg_solve(bs_ctx *ctx, const bs_gs_dev *t, const double *dL, const double *bG, double *xG,
+                double *rG, double *pG, double *ApG, int32_t iters, double *scal_dev,
+                void *stream);
 
 /* ---- diagnostics ----------------------------------------------------------
  * Throughput probe of the binary64 fused multiply-add pipe: launches

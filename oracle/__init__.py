@@ -168,6 +168,13 @@ def apply_diag(ids, dL, xG):
     return gather(ids, _f64(dL) * qL, np.asarray(xG).size)
 
 
+def _quot(num, den):
+    """A CG coefficient num / den, or 0 where den is 0 (reading: a vanishing
+    p.Ap or r.r occurs only at an exact solution, where a zero step keeps x;
+    the pages do not say)."""
+    return float(num) / float(den) if float(den) != 0.0 else 0.0
+
+
 def cg_sequence(ids, pG, xG, rG, rr):
     """One CG iteration's streaming sequence with the identity local operator.
 
@@ -179,7 +186,50 @@ def cg_sequence(ids, pG, xG, rG, rr):
     pL = scatter(ids, pG)
     ApG = gather(ids, pL, pG.size)
     pAp = dot(pG, ApG)
-    alpha = float(rr) / pAp
+    alpha = _quot(rr, pAp)
     x1, r1, rr_new = cg_update(alpha, pG, ApG, xG, rG)
     rnorm = norm(r1)
     return dict(pL=pL, ApG=ApG, pAp=pAp, alpha=alpha, x=x1, r=r1, rr_new=rr_new, rnorm=rnorm)
+
+
+def cg_solve(ids, dL, bG, xG, iters):
+    """Conjugate gradients on A = Z^T diag(dL) Z (dL None: A = Z^T Z).
+
+    "Portable high-order finite element kernels I": each benchmark problem
+    solves its system by CG (Algorithm 1), whose vector operations are
+    y = alpha x + beta y, dot, norm and y = A x, and whose steps 8-10 (the x
+    update, the r update and r.r) fuse into BS5.  The listing itself was
+    lost; this is the textbook (Hestenes-Stiefel) iteration with exactly
+    those operations, in that order:
+
+        r = b - A x  (BS2 with alpha = -1);  p = r;  rr_0 = r.r
+        for k < iters:
+            Ap = A p;  pAp_k = p.Ap;  alpha = rr_k / pAp_k
+            x += alpha p;  r -= alpha Ap;  rr_{k+1} = r.r      (BS5)
+            p = r + (rr_{k+1} / rr_k) p                        (BS2, alpha = 1)
+
+    A quotient with a zero denominator is 0 (see _quot).  Returns a dict
+    with x, r, p (after the last iteration), rr [iters + 1] and pAp [iters].
+    """
+    bG = _f64(bG)
+    NG = bG.size
+    ids = _i32(ids)
+
+    def A(v):
+        if dL is None:
+            return gather(ids, scatter(ids, v), NG)
+        return apply_diag(ids, dL, v)
+
+    x = np.array(xG, dtype=np.float64, copy=True, order="C")
+    assert x.size == NG
+    r = axpy(-1.0, A(x), 1.0, bG)
+    p = copy(r)
+    rr = [norm(r)]
+    pAp = []
+    for k in range(int(iters)):
+        Ap = A(p)
+        pAp.append(dot(p, Ap))
+        x, r, rr_new = cg_update(_quot(rr[k], pAp[k]), p, Ap, x, r)
+        rr.append(rr_new)
+        p = axpy(1.0, r, _quot(rr_new, rr[k]), p)
+    return dict(x=x, r=r, p=p, rr=rr, pAp=pAp)

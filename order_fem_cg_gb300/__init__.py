@@ -44,7 +44,7 @@ EXPORTS = (
     "bs_mesh_build_box", "bs_mesh_build_box_ex", "bs_mesh_info", "bs_mesh_tables",
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
     "bs_probe_dfma", "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
-    "bs_apply_diag",
+    "bs_apply_diag", "bs_axpy_dev", "bs_cg_solve",
 )
 
 
@@ -120,6 +120,9 @@ def _declare(lib):
         "bs_scatter": ([_vp, ctypes.POINTER(GSDev), _vp, _vp, _vp], _int),
         "bs_cg_iteration": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 10, _int),
         "bs_apply_diag": ([_vp, ctypes.POINTER(GSDev), _vp, _vp, _vp, _vp], _int),
+        "bs_axpy_dev": ([_vp, _i64, _dbl, _vp, _vp, _vp, _vp, _vp], _int),
+        "bs_cg_solve": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 6 + [ctypes.c_int32, _vp, _vp],
+                        _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
         "bs_mesh_plan": ([_vp] + [ctypes.c_int32] * 5, _int),
@@ -246,6 +249,16 @@ def bs_axpy(alpha, x, beta, y, stream=None, ctx=None):
     ctx = _ctx(ctx, x)
     ctx.check(lib.bs_axpy(ctx.handle, x.numel(), float(alpha), _vec(x, "x"), float(beta),
                           _vec(y, "y", x.numel()), _stream(stream)), "bs_axpy")
+    return y
+
+
+def bs_axpy_dev(alpha, x, beta_num, beta_den, y, stream=None, ctx=None):
+    """BS2 with beta = beta_num[0] / beta_den[0] formed on the device (0 if
+    the denominator is 0): y <- fma(alpha, x, beta * y)."""
+    ctx = _ctx(ctx, x)
+    ctx.check(lib.bs_axpy_dev(ctx.handle, x.numel(), float(alpha), _vec(x, "x"),
+                              _vec(beta_num, "beta_num"), _vec(beta_den, "beta_den"),
+                              _vec(y, "y", x.numel()), _stream(stream)), "bs_axpy_dev")
     return y
 
 
@@ -498,12 +511,30 @@ def bs_scatter(tables, qG, qL, stream=None, ctx=None):
 
 
 def bs_apply_diag(tables, xG, dL, yG, stream=None, ctx=None):
-    """yG <- Z^T (dL .* (Z xG)): the global operator of a diagonal local operator (fused)."""
+    """yG <- Z^T (dL .* (Z xG)): the global operator of a diagonal local operator
+    (fused); dL None is the identity local operator (yG <- Z^T Z xG)."""
     ctx = _ctx(ctx, xG)
     ctx.check(lib.bs_apply_diag(ctx.handle, ctypes.byref(tables.struct), _vec(xG, "xG", tables.NG),
-                                _vec(dL, "dL", tables.NL), _vec(yG, "yG", tables.NG),
-                                _stream(stream)), "bs_apply_diag")
+                                _vec(dL, "dL", tables.NL) if dL is not None else _vp(0),
+                                _vec(yG, "yG", tables.NG), _stream(stream)), "bs_apply_diag")
     return yG
+
+
+def bs_cg_solve(tables, dL, bG, xG, rG, pG, ApG, iters, scal=None, stream=None, ctx=None):
+    """`iters` CG iterations on A = Z^T diag(dL) Z (dL None: Z^T Z), from xG
+    (updated in place), every scalar on the device.  Returns scal
+    [2 iters + 1]: rr_0 .. rr_iters, then pAp_0 .. pAp_{iters-1}."""
+    ctx = _ctx(ctx, bG)
+    NG = tables.NG
+    iters = int(iters)
+    if scal is None:
+        scal = torch.empty(2 * iters + 1, dtype=torch.float64, device=bG.device)
+    ctx.check(lib.bs_cg_solve(
+        ctx.handle, ctypes.byref(tables.struct),
+        _vec(dL, "dL", tables.NL) if dL is not None else _vp(0), _vec(bG, "bG", NG),
+        _vec(xG, "xG", NG), _vec(rG, "rG", NG), _vec(pG, "pG", NG), _vec(ApG, "ApG", NG),
+        iters, _vec(scal, "scal", 2 * iters + 1), _stream(stream)), "bs_cg_solve")
+    return scal
 
 
 def bs_cg_iteration(tables, pG, pL, ApG, xG, rG, rr, pAp, rr_new, rnorm, stream=None, ctx=None):

@@ -351,6 +351,52 @@ extern "C" int bs_cg_iteration(bs_ctx *ctx, const bs_gs_dev *t, const double *pG
     return bs_norm(ctx, n, rG, rnorm_dev, stream);
 }
 
+extern "C" int bs_cg_solve(bs_ctx *ctx, const bs_gs_dev *t, const double *dL, const double *bG,
+                           double *xG, double *rG, double *pG, double *ApG, int32_t iters,
+                           double *scal_dev, void *stream)
+{
+    if (!ctx)
+        return BS_EINVAL;
+    if (!t || iters < 0 || !scal_dev)
+        return bs_set_error(ctx, BS_EINVAL, "bs_cg_solve: NULL tables/scalars or iters < 0");
+    const int64_t n = t->NG;
+    if (n > 0 && (!bG || !xG || !rG || !pG || !ApG))
+        return bs_set_error(ctx, BS_EINVAL, "bs_cg_solve: NULL vector");
+    const double *vin[2] = {bG, xG};
+    double *vout[3] = {rG, pG, ApG};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 2; ++j)
+            if (bs_overlap(vout[i], 8 * n, vin[j], 8 * n))
+                return bs_set_error(ctx, BS_EINVAL, "bs_cg_solve: work vectors overlap b or x");
+        for (int j = i + 1; j < 3; ++j)
+            if (bs_overlap(vout[i], 8 * n, vout[j], 8 * n))
+                return bs_set_error(ctx, BS_EINVAL, "bs_cg_solve: r, p and Ap overlap");
+        if (bs_overlap(vout[i], 8 * n, scal_dev, 8 * (2ll * iters + 1)))
+            return bs_set_error(ctx, BS_EINVAL, "bs_cg_solve: scalars overlap a vector");
+    }
+    if (bs_overlap(bG, 8 * n, xG, 8 * n))
+        return bs_set_error(ctx, BS_EINVAL, "bs_cg_solve: b and x overlap");
+    double *rr = scal_dev, *pAp = scal_dev + iters + 1;
+    int st;
+    // r = b - A x; p = r; rr_0 = r.r
+    if ((st = bs_apply_diag(ctx, t, xG, dL, ApG, stream)) ||
+        (st = bs_copy(ctx, n, bG, rG, stream)) ||
+        (st = bs_axpy(ctx, n, -1.0, ApG, 1.0, rG, stream)) ||
+        (st = bs_copy(ctx, n, rG, pG, stream)) || (st = bs_norm(ctx, n, rG, rr, stream)))
+        return st;
+    for (int32_t k = 0; k < iters; ++k) {
+        // Ap = A p; alpha = rr_k / p.Ap; x += alpha p, r -= alpha Ap, rr_k+1 = r.r;
+        // p = r + (rr_k+1 / rr_k) p
+        if ((st = bs_apply_diag(ctx, t, pG, dL, ApG, stream)) ||
+            (st = bs_dot(ctx, n, pG, ApG, pAp + k, stream)) ||
+            (st = bs_cg_update(ctx, n, rr + k, pAp + k, 0.0, pG, ApG, xG, rG, rr + k + 1,
+                               stream)) ||
+            (st = bs_axpy_dev(ctx, n, 1.0, rG, rr + k + 1, rr + k, pG, stream)))
+            return st;
+    }
+    return BS_OK;
+}
+
 extern "C" int bs_apply_diag(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, const double *dL,
                              double *yG, void *stream)
 {
@@ -360,9 +406,10 @@ extern "C" int bs_apply_diag(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, 
         return st;
     if (!t->plan)
         return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: needs a two-pass plan");
-    if ((t->NG > 0 && (!xG || !yG)) || (t->NL > 0 && !dL))
+    if (t->NG > 0 && (!xG || !yG))
         return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: NULL vector");
-    if (bs_overlap(xG, 8 * t->NG, yG, 8 * t->NG) || bs_overlap(dL, 8 * t->NL, yG, 8 * t->NG))
+    if (bs_overlap(xG, 8 * t->NG, yG, 8 * t->NG) ||
+        (dL && bs_overlap(dL, 8 * t->NL, yG, 8 * t->NG)))
         return bs_set_error(ctx, BS_EINVAL, "bs_apply_diag: yG overlaps xG or dL");
     if ((reinterpret_cast<uintptr_t>(xG) | reinterpret_cast<uintptr_t>(dL) |
          reinterpret_cast<uintptr_t>(yG)) & 7u)

@@ -941,8 +941,9 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
 // bucket u and gather tile u (the plan has s_bucket_len == g_tile_len and
 // one block per cluster).  It places scatter bucket u's runs (read from
 // `ws`) in shared memory -- that is q_L = Z x on the range, masked locals
-// +0.0 --, multiplies by d_L, and emits gather tile u's runs into `wg`
-// directly, so q_L never reaches HBM.
+// +0.0 --, multiplies by d_L (skipped for dL == nullptr: the identity local
+// operator), and emits gather tile u's runs into `wg` directly, so q_L
+// never reaches HBM.
 __global__ void __launch_bounds__(kT, 1)
     fused_diag_kernel(PlanArgs a, const double *__restrict__ ws, const double *__restrict__ dL,
                       double *__restrict__ wg)
@@ -990,7 +991,7 @@ __global__ void __launch_bounds__(kT, 1)
     // (commit_runs begins with a barrier: the placements are complete after it)
     ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
          run_off(runs[a.g_nbuckets]) == s1 - s0;
-    if (ok) {
+    if (ok && dL) {
         for (int32_t i0 = threadIdx.x; i0 < len; i0 += kU * kT) {
             double w[kU];
 #pragma unroll

@@ -277,12 +277,30 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const double *__restrict
     }
 }
 
+// num / den, or 0 where den is 0: a device-side CG coefficient (rr / pAp or
+// rr_new / rr) whose denominator vanishes only once the iteration has met
+// an exact solution, where a zero step keeps it.
+__device__ __forceinline__ double dev_quotient(const double *num, const double *den)
+{
+    const double d = den[0];
+    return d != 0.0 ? __ddiv_rn(num[0], d) : 0.0;
+}
+
 // ---------------------------------------------------------------- BS2 AXPY
+// beta = beta_num[0] / beta_den[0] (dev_quotient) when beta_num is given.
 template <int V, int UNROLL, bool BETA1>
 __global__ void __launch_bounds__(kThreads) axpy_kernel(double alpha, const double *x, double beta,
                                                         double *y, int64_t h, int64_t nv,
-                                                        int64_t t)
+                                                        int64_t t, const double *beta_num,
+                                                        const double *beta_den)
 {
+    if (!BETA1 && beta_num) {
+        __shared__ double s_beta;
+        if (threadIdx.x == 0)
+            s_beta = dev_quotient(beta_num, beta_den);
+        __syncthreads();
+        beta = s_beta;
+    }
     const int64_t gid = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const double *xv = x + h;
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(kThreads)
     double alpha = alpha_host;
     if (alpha_num) {
         if (threadIdx.x == 0)
-            s_alpha = __ddiv_rn(alpha_num[0], alpha_den[0]);
+            s_alpha = dev_quotient(alpha_num, alpha_den);
         __syncthreads();
         alpha = s_alpha;
     }
@@ -529,12 +547,14 @@ void launch_copy(int grid, cudaStream_t s, const double *x, double *y, const Pla
 
 template <int V>
 void launch_axpy(int grid, cudaStream_t s, double a, const double *x, double b, double *y,
-                 const Plan &pl)
+                 const Plan &pl, const double *bnum, const double *bden)
 {
-    if (b == 1.0)
-        axpy_kernel<V, kStreamUnroll, true><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv, pl.t);
+    if (b == 1.0 && !bnum)
+        axpy_kernel<V, kStreamUnroll, true><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv, pl.t,
+                                                                      nullptr, nullptr);
     else
-        axpy_kernel<V, kStreamUnroll, false><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv, pl.t);
+        axpy_kernel<V, kStreamUnroll, false><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv,
+                                                                       pl.t, bnum, bden);
 }
 
 template <int V, bool DOT>
@@ -595,19 +615,22 @@ extern "C" int bs_copy(bs_ctx *ctx, int64_t n, const double *x, double *y, void 
     return BS_OK;
 }
 
-extern "C" int bs_axpy(bs_ctx *ctx, int64_t n, double alpha, const double *x, double beta,
-                       double *y, void *stream)
+static int axpy_common(bs_ctx *ctx, const char *name, int64_t n, double alpha, const double *x,
+                       double beta, const double *bnum, const double *bden, double *y,
+                       void *stream)
 {
     if (!ctx)
         return BS_EINVAL;
     if (n < 0 || (n > 0 && (!x || !y)))
-        return bs_set_error(ctx, BS_EINVAL, "bs_axpy: bad length or NULL pointer");
+        return bs_set_error(ctx, BS_EINVAL, "%s: bad length or NULL pointer", name);
     if (n == 0)
         return BS_OK;
-    if (!aligned8(x) || !aligned8(y))
-        return bs_set_error(ctx, BS_EINVAL, "bs_axpy: pointers must be 8-byte aligned");
+    if (!aligned8(x) || !aligned8(y) || (bnum && (!aligned8(bnum) || !aligned8(bden))))
+        return bs_set_error(ctx, BS_EINVAL, "%s: pointers must be 8-byte aligned", name);
     if (x != y && bs_overlap(x, 8 * n, y, 8 * n))
-        return bs_set_error(ctx, BS_EINVAL, "bs_axpy: x and y overlap");
+        return bs_set_error(ctx, BS_EINVAL, "%s: x and y overlap", name);
+    if (bnum && (bs_overlap(bnum, 8, y, 8 * n) || bs_overlap(bden, 8, y, 8 * n)))
+        return bs_set_error(ctx, BS_EINVAL, "%s: beta scalars overlap y", name);
     if (int st = bs_check_device(ctx))
         return st;
     const void *ps[2] = {x, y};
@@ -615,12 +638,28 @@ extern "C" int bs_axpy(bs_ctx *ctx, int64_t n, double alpha, const double *x, do
     const int grid = grid_for(ctx, ctx->tune.stream_blocks_per_sm, (pl.nv + 1) / 2, 1 << 30);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (pl.V) {
-    case 4: launch_axpy<4>(grid, s, alpha, x, beta, y, pl); break;
-    case 2: launch_axpy<2>(grid, s, alpha, x, beta, y, pl); break;
-    default: launch_axpy<1>(grid, s, alpha, x, beta, y, pl); break;
+    case 4: launch_axpy<4>(grid, s, alpha, x, beta, y, pl, bnum, bden); break;
+    case 2: launch_axpy<2>(grid, s, alpha, x, beta, y, pl, bnum, bden); break;
+    default: launch_axpy<1>(grid, s, alpha, x, beta, y, pl, bnum, bden); break;
     }
     BS_LAUNCH_CHECK(ctx, "axpy_kernel");
     return BS_OK;
+}
+
+extern "C" int bs_axpy(bs_ctx *ctx, int64_t n, double alpha, const double *x, double beta,
+                       double *y, void *stream)
+{
+    return axpy_common(ctx, "bs_axpy", n, alpha, x, beta, nullptr, nullptr, y, stream);
+}
+
+extern "C" int bs_axpy_dev(bs_ctx *ctx, int64_t n, double alpha, const double *x,
+                           const double *beta_num_dev, const double *beta_den_dev, double *y,
+                           void *stream)
+{
+    if (ctx && (!beta_num_dev || !beta_den_dev))
+        return bs_set_error(ctx, BS_EINVAL, "bs_axpy_dev: NULL beta scalar");
+    return axpy_common(ctx, "bs_axpy_dev", n, alpha, x, 0.0, beta_num_dev, beta_den_dev, y,
+                       stream);
 }
 
 static int dot_common(bs_ctx *ctx, const char *name, int64_t n, const double *x, const double *y,

@@ -475,3 +475,126 @@ def test_planted_mass_operator_mistakes_are_caught():
     for wrong in mutants:
         with pytest.raises(AssertionError):
             _check_mass_operator(wrong, cfg, ids)
+
+
+# ----------------------------------------------------------------------------
+# Conjugate gradients (textbook iteration on Z^T diag(d) Z)
+# ----------------------------------------------------------------------------
+# Z^T diag(d) Z is diagonal (entry g: the sum of d over the local copies of
+# node g), so the exact solution is b / gather(d), and CG on it terminates
+# in as many steps as the diagonal has distinct values (with nonzero b
+# components): facts of the method, not of the oracle's code.
+
+def _cg_mesh(E=3, N=3, seed=12345):
+    cfg = gen.MeshConfig("t", E, N, seed, gen.SHUFFLE_ELEMS | gen.PERMUTE_GLOBAL)
+    ep, npm = gen.mesh_perms(cfg)
+    return cfg, oracle.box_scatter_ids(E, N, ep, npm)
+
+
+def test_cg_identity_operator_terminates_in_four_steps():
+    """Z^T Z = diag(multiplicity), multiplicities {1, 2, 4, 8}: four steps."""
+    cfg = gen.WORKLOADS["tiny"]
+    ep, npm = gen.mesh_perms(cfg)
+    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm)
+    m = oracle.gather(ids, np.ones(cfg.NL), cfg.NG)
+    assert sorted(np.unique(m).tolist()) == [1.0, 2.0, 4.0, 8.0]
+    b = gen.uniform_pm1(cfg.seed, gen.TAG_R, cfg.NG)
+    res = oracle.cg_solve(ids, None, b, np.zeros(cfg.NG), 4)
+    rr = np.array(res["rr"])
+    assert np.all(rr[:4] > 1e-6 * rr[0]) and rr[4] < 1e-28 * rr[0]
+    assert np.max(np.abs(res["x"] - b / m)) <= 1e-14 * np.max(np.abs(b))
+
+
+def test_cg_mass_operator_terminates_at_distinct_eigenvalue_count():
+    cfg, ids = _cg_mesh(3, 3)
+    d = gen.mass_diagonal(cfg.E, cfg.N)
+    diag = oracle.gather(ids, d, cfg.NG)
+    nd = np.unique(np.round(diag / diag.max(), 12)).size
+    assert nd == 10
+    b = gen.uniform_pm1(7, 1, cfg.NG)
+    res = oracle.cg_solve(ids, d, b, np.zeros(cfg.NG), nd + 1)
+    rr = np.array(res["rr"])
+    assert np.all(rr[:nd] > 1e-7 * rr[0]) and rr[nd] < 1e-8 * rr[0]
+    xs = b / diag
+    assert np.max(np.abs(res["x"] - xs)) <= 1e-9 * np.max(np.abs(xs))
+
+
+def _check_cg(solve, iters=8, E=3, N=3, x0_seed=None):
+    """Textbook CG properties of solve(ids, d, b, x0, k) for k = 0..iters on the
+    mass operator: the recursive residual is b - A x_k, residuals are mutually
+    orthogonal, directions A-conjugate (both up to the slow loss of
+    orthogonality of finite-precision CG, ~1e-8 here; a wrong step breaks
+    them at O(1)), the A-norm error decreases and obeys
+    2 ((sqrt(kappa) - 1) / (sqrt(kappa) + 1))^k, and rr_k = r_k . r_k."""
+    cfg, ids = _cg_mesh(E, N)
+    d = gen.mass_diagonal(cfg.E, cfg.N)
+    diag = oracle.gather(ids, d, cfg.NG)
+    b = gen.uniform_pm1(7, 1, cfg.NG)
+    x0 = np.zeros(cfg.NG) if x0_seed is None else gen.uniform_pm1(x0_seed, 2, cfg.NG)
+    xs = b / diag
+    kappa = diag.max() / diag.min()
+    rho = (math.sqrt(kappa) - 1) / (math.sqrt(kappa) + 1)
+    runs = [solve(ids, d, b, x0, k) for k in range(iters + 1)]
+    err = [math.sqrt(math.fsum(diag * (xs - r_["x"]) ** 2)) for r_ in runs]
+    bmax = np.max(np.abs(b))
+    for k, r_ in enumerate(runs):
+        true_r = b - diag * r_["x"]
+        assert np.max(np.abs(true_r - r_["r"])) <= 1e-12 * bmax, k
+        assert abs(r_["rr"][k] - math.fsum(r_["r"] ** 2)) <= 1e-13 * r_["rr"][k], k
+        assert err[k] <= 2 * rho ** k * err[0] * (1 + 1e-9), k
+        if k:
+            assert err[k] <= err[k - 1] * (1 + 1e-12), k
+    R = [r_["r"] for r_ in runs]
+    P = [r_["p"] for r_ in runs]
+    for i in range(iters + 1):
+        for j in range(i + 1, iters + 1):
+            ri, rj = math.fsum(R[i] ** 2), math.fsum(R[j] ** 2)
+            assert abs(math.fsum(R[i] * R[j])) <= 1e-6 * math.sqrt(ri * rj), (i, j)
+            pi, pj = math.fsum(diag * P[i] ** 2), math.fsum(diag * P[j] ** 2)
+            assert abs(math.fsum(P[i] * diag * P[j])) <= 1e-6 * math.sqrt(pi * pj), (i, j)
+
+
+def test_cg_textbook_properties():
+    _check_cg(oracle.cg_solve)
+    _check_cg(oracle.cg_solve, iters=5, x0_seed=11)
+
+
+def _cg_mutant(which):
+    """The textbook loop rebuilt from oracle steps with one planted mistake."""
+    def solve(ids, d, b, x0, iters):
+        NG = b.size
+        A = lambda v: oracle.apply_diag(ids, d, v)                     # noqa: E731
+        x = np.array(x0, dtype=np.float64)
+        r = oracle.axpy(-1.0, A(x), 1.0, b)
+        p = oracle.copy(r)
+        rr = [oracle.norm(r)]
+        for k in range(iters):
+            Ap = A(p)
+            pAp = oracle.dot(p, Ap)
+            alpha = rr[k] / pAp if which != "alpha_inverted" else pAp / rr[k]
+            if which == "x_along_r":
+                x = oracle.axpy(alpha, r, 1.0, x)
+                r = oracle.axpy(-alpha, Ap, 1.0, r)
+                rrn = oracle.norm(r)
+            else:
+                x, r, rrn = oracle.cg_update(alpha, p, Ap, x, r)
+            if which == "r_sign":
+                r = oracle.axpy(2 * alpha, Ap, 1.0, r)
+                rrn = oracle.norm(r)
+            rr.append(rrn)
+            beta = {"beta_inverted": rr[k] / rrn, "no_beta": 0.0}.get(which, rrn / rr[k])
+            p = oracle.axpy(1.0, r, beta if which != "p_minus" else -beta, p)
+        assert len(rr) == iters + 1 and NG == x.size
+        return dict(x=x, r=r, p=p, rr=rr)
+    return solve
+
+
+@pytest.mark.parametrize("which", ["alpha_inverted", "x_along_r", "r_sign", "beta_inverted",
+                                   "no_beta", "p_minus"])
+def test_planted_cg_mistakes_are_caught(which):
+    with pytest.raises(AssertionError):
+        _check_cg(_cg_mutant(which), iters=6)
+
+
+def test_cg_mutant_harness_without_mistake_passes():
+    _check_cg(_cg_mutant("none"), iters=6)
