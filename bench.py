@@ -382,7 +382,9 @@ class OracleSample:
         self.oracle = oracle
         self.cfg = cfg
         ep, npm = gen.mesh_perms(cfg)
-        self.ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+        orient = gen.element_orientations(cfg) if cfg.flags & gen.ROTATE_ELEMS else None
+        self.ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY),
+                                          orient)
         NL, NG = cfg.NL, cfg.NG
         self.m = max(1, int(NL * frac))
         self.mg = max(1, int(NG * frac))
@@ -456,10 +458,19 @@ def run_reference(args):
     return 0
 
 
+def mesh_numbering(cfg):
+    """Plain words for a mesh workload's numbering flags."""
+    parts = [("elements shuffled", gen.SHUFFLE_ELEMS), ("global ids permuted", gen.PERMUTE_GLOBAL),
+             ("elements randomly oriented", gen.ROTATE_ELEMS),
+             ("boundary nodes masked (Dirichlet)", gen.MASK_BOUNDARY)]
+    on = [w for w, f in parts if cfg.flags & f]
+    return ", ".join(on) if on else "lattice numbering"
+
+
 def workload_config(cfg, gpus, planned=None):
     out = {
         "workload": f"{cfg.name} box mesh E={cfg.E} N={cfg.N}: {cfg.K} hexahedra, N_L={cfg.NL} local "
-                    f"and N_G={cfg.NG} global nodes, elements shuffled and global ids permuted by "
+                    f"and N_G={cfg.NG} global nodes, {mesh_numbering(cfg)} by "
                     f"seed {cfg.seed:#x}; fp64 U(-1,1) data, alpha={cfg.alpha}, beta={cfg.beta}; step = "
                     "BS1-BS5 at n=N_L, BS6 gather, BS7 scatter, one CG iteration's sequence at n=N_G",
         "l2": (f"inputs larger than L2: every operation streams its own buffers of >= "

@@ -51,6 +51,7 @@ TAG_R = 6
 TAG_X = 7
 TAG_ALPHA = 8
 TAG_Y = 9
+TAG_ORIENT = 10
 # Tags >= 16 are free for extra vectors a caller needs (e.g. one distinct
 # buffer per operation in a timed step).
 TAG_EXTRA = 16
@@ -61,6 +62,7 @@ SEED_BASE = 0xB5EED000
 SHUFFLE_ELEMS = 1
 PERMUTE_GLOBAL = 2
 MASK_BOUNDARY = 4
+ROTATE_ELEMS = 8
 
 
 def mix64_int(z: int) -> int:
@@ -170,12 +172,16 @@ class MeshConfig:
 
 
 # The benchmark workloads: four box meshes (tiny, mid, large, stress) and the
-# vector-length sweep 2^10 .. 2^27 for the five mesh-free operations.
+# vector-length sweep 2^10 .. 2^27 for the five mesh-free operations; plus
+# the stress mesh with Dirichlet-masked boundary nodes and randomly oriented
+# elements (an unstructured-like numbering) at the same scale.
 WORKLOADS = {
     "tiny": MeshConfig("tiny", 8, 3, SEED_BASE + 0),
     "mid": MeshConfig("mid", 20, 7, SEED_BASE + 1),
     "large": MeshConfig("large", 32, 7, SEED_BASE + 3),
     "stress": MeshConfig("stress", 64, 5, SEED_BASE + 4),
+    "stress_masked": MeshConfig("stress_masked", 64, 5, SEED_BASE + 5,
+                                SHUFFLE_ELEMS | PERMUTE_GLOBAL | MASK_BOUNDARY | ROTATE_ELEMS),
 }
 SWEEP_SEED = SEED_BASE + 2
 SWEEP_LOG2 = tuple(range(10, 28))
@@ -196,6 +202,18 @@ def mesh_perms(cfg: MeshConfig):
     else:
         npm = np.arange(cfg.NG, dtype=np.int32)
     return ep, npm
+
+
+def element_orientations(cfg: MeshConfig) -> np.ndarray:
+    """Orientation index in [0, 24) of every lattice element (uint8), drawn
+    as ((z_e >> 11) * 24) >> 53 from stream (seed, TAG_ORIENT); zeros when
+    the ROTATE_ELEMS flag is off.  (The rotation an index names is part of
+    the mesh numbering, implemented by each table builder.)"""
+    if not cfg.flags & ROTATE_ELEMS:
+        return np.zeros(cfg.K, dtype=np.uint8)
+    z = draws(cfg.seed, TAG_ORIENT, cfg.K) >> np.uint64(11)
+    with np.errstate(over="ignore"):
+        return ((z * np.uint64(24)) >> np.uint64(53)).astype(np.uint8)
 
 
 def gll_nodes_weights(N: int):

@@ -60,6 +60,7 @@ extern "C" {
 #define BS_MESH_SHUFFLE_ELEMS 1u   /* seeded random order of elements in storage */
 #define BS_MESH_PERMUTE_GLOBAL 2u  /* seeded random global node numbering        */
 #define BS_MESH_MASK_BOUNDARY 4u   /* boundary local nodes get id -1 (masked)    */
+#define BS_MESH_ROTATE_ELEMS 8u    /* seeded random orientation of every element */
 
 /* Largest number of CSR entries in one gather row segment the gather kernel
  * can stage in shared memory. */
@@ -200,12 +201,19 @@ int bs_cg_update(bs_ctx *ctx, int64_t n, const double *alpha_num_dev,
  * N_L = K (p+1)^3).  Lattice element (ex,ey,ez) is number ex + E(ey + E ez);
  * storage slot s holds lattice element elemPerm[s]; local node (i,j,k) of
  * slot s has local index s (N+1)^3 + i + (N+1)(j + (N+1)k) and lies on
- * lattice node (ex N + i, ey N + j, ez N + k), numbered x fastest on the
- * (EN+1)^3 lattice; its global id is nodePerm[lattice number].
+ * lattice node (ex N + w0, ey N + w1, ez N + w2), numbered x fastest on the
+ * (EN+1)^3 lattice, with w = (i, j, k) rotated by the element's orientation
+ * (identity unless ROTATE_ELEMS); its global id is nodePerm[lattice number].
  * Permutations (flags SHUFFLE_ELEMS / PERMUTE_GLOBAL, else identity): the
  * indices 0..n-1 ordered by (z_i, i), z_i the i-th SplitMix64 output from
  * state seed XOR (tag * 0x9E3779B97F4A7C15), tag 1 for elements, 2 for
- * global nodes.
+ * global nodes.  Orientations (ROTATE_ELEMS): lattice element e takes
+ * rotation ((z_e >> 11) * 24) >> 53 of stream tag 10, an index into the 24
+ * proper rotations of the cube ordered by axis permutation (lexicographic:
+ * output axis a takes input axis perm[a]) and then flip mask f = 0..7 (bit
+ * a reverses output axis a, w_a = N - v[perm[a]]), keeping determinant +1;
+ * rotation 0 is the identity.  MASK_BOUNDARY masks the local nodes on the
+ * box boundary (-1), rotated or not.
  * Tables: scatterIds (local -> global, "scatterIds", negative = masked),
  * the CSR of Z^T with rows in global-id order and each row's local ids
  * ascending, and blockStarts grouping consecutive rows into segments of at

@@ -68,7 +68,7 @@ def _load():
         lib.oracle_scatter.argtypes = [_i64, _i32p, _f64p, _f64p]
         lib.oracle_gather.argtypes = [_i64, _i64, _i32p, _f64p, _f64p]
         lib.oracle_box_scatter_ids.argtypes = [ctypes.c_int, ctypes.c_int, _i32p, _i32p,
-                                               ctypes.c_int, _i32p]
+                                               ctypes.c_int, ctypes.c_void_p, _i32p]
         for f in (lib.oracle_copy, lib.oracle_axpy, lib.oracle_cg_update, lib.oracle_scatter,
                   lib.oracle_gather, lib.oracle_box_scatter_ids):
             f.restype = None
@@ -150,12 +150,17 @@ def gather(ids, qL, NG):
     return qG
 
 
-def box_scatter_ids(E, N, elem_perm, node_perm, mask_boundary=False):
-    """Local-to-global table of an E^3 box mesh of degree N (int32, -1 = masked)."""
+def box_scatter_ids(E, N, elem_perm, node_perm, mask_boundary=False, orient=None):
+    """Local-to-global table of an E^3 box mesh of degree N (int32, -1 = masked);
+    orient[e] in [0, 24) rotates lattice element e's local numbering."""
     ep, npm = _i32(elem_perm), _i32(node_perm)
     assert ep.size == E ** 3 and npm.size == (E * N + 1) ** 3
     ids = np.empty(E ** 3 * (N + 1) ** 3, dtype=np.int32)
-    _load().oracle_box_scatter_ids(int(E), int(N), ep, npm, int(bool(mask_boundary)), ids)
+    if orient is not None:
+        orient = np.ascontiguousarray(orient, dtype=np.uint8)
+        assert orient.size == E ** 3 and int(orient.max(initial=0)) < 24
+    _load().oracle_box_scatter_ids(int(E), int(N), ep, npm, int(bool(mask_boundary)),
+                                   orient.ctypes.data if orient is not None else None, ids)
     return ids
 
 

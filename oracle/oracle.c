@@ -111,19 +111,47 @@ void oracle_gather(int64_t NL, int64_t NG, const int32_t *ids, const double *qL,
             qG[ids[l]] += qL[l];
 }
 
+/* The 24 proper rotations of the reference cube, in a fixed order (mesh
+ * numbering convention): the axis permutations pi of (0, 1, 2) in
+ * lexicographic order, and for each the flip masks f = 0 .. 7 (bit a:
+ * output axis a reversed), keeping those whose signed permutation matrix
+ * has determinant sign(pi) (-1)^popcount(f) = +1.  Index 0 is the identity. */
+static void cube_rotations(int perm[24][3], int flip[24][3])
+{
+    static const int P[6][3] = {{0, 1, 2}, {0, 2, 1}, {1, 0, 2}, {1, 2, 0}, {2, 0, 1}, {2, 1, 0}};
+    static const int sign[6] = {1, -1, -1, 1, 1, -1};
+    int o = 0;
+    for (int p = 0; p < 6; ++p)
+        for (int f = 0; f < 8; ++f) {
+            int flips = (f & 1) + ((f >> 1) & 1) + ((f >> 2) & 1);
+            if (sign[p] * ((flips & 1) ? -1 : 1) != 1)
+                continue;
+            for (int a = 0; a < 3; ++a) {
+                perm[o][a] = P[p][a];
+                flip[o][a] = (f >> a) & 1;
+            }
+            ++o;
+        }
+}
+
 /* Box-mesh local-to-global table [P1, eq. (1) K hexahedra, (p+1)^3 GLL
  * nodes per element, N_L = K(p+1)^3; P2, I_{l->g}].
  *
  * The mesh is E x E x E hexahedra of degree N on a box.  Lattice element
  * (ex, ey, ez) has number ex + E (ey + E ez).  Storage slot s holds lattice
- * element elemPerm[s].  Its local node (i, j, k), 0 <= i, j, k <= N, has
- * local index l = s (N+1)^3 + i + (N+1)(j + (N+1) k) and sits on lattice
- * node (ex N + i, ey N + j, ez N + k) of the (E N + 1)^3 lattice, numbered
- * x fastest; that lattice node's global id is nodePerm[lattice number].
- * With mask_boundary != 0 every local node on the box boundary gets -1. */
+ * element e = elemPerm[s], with orientation o = orient[e] (0 if orient is
+ * NULL).  Its local node (i, j, k), 0 <= i, j, k <= N, has local index
+ * l = s (N+1)^3 + i + (N+1)(j + (N+1) k); with v = (i, j, k) and rotation o
+ * of cube_rotations, w_a = v[perm_a], or N - v[perm_a] if axis a is
+ * flipped, and the node sits on lattice node (ex N + w_0, ey N + w_1,
+ * ez N + w_2) of the (E N + 1)^3 lattice, numbered x fastest; that lattice
+ * node's global id is nodePerm[lattice number].  With mask_boundary != 0
+ * every local node on the box boundary gets -1. */
 void oracle_box_scatter_ids(int E, int N, const int32_t *elemPerm, const int32_t *nodePerm,
-                            int mask_boundary, int32_t *ids)
+                            int mask_boundary, const uint8_t *orient, int32_t *ids)
 {
+    int perm[24][3], flip[24][3];
+    cube_rotations(perm, flip);
     int64_t K = (int64_t)E * E * E;
     int64_t q = N + 1;
     int64_t M = (int64_t)E * N + 1;
@@ -132,10 +160,14 @@ void oracle_box_scatter_ids(int E, int N, const int32_t *elemPerm, const int32_t
         int64_t ex = e % E;
         int64_t ey = (e / E) % E;
         int64_t ez = e / ((int64_t)E * E);
+        int o = orient ? orient[e] : 0;
         for (int64_t k = 0; k < q; ++k)
             for (int64_t j = 0; j < q; ++j)
                 for (int64_t i = 0; i < q; ++i) {
-                    int64_t gx = ex * N + i, gy = ey * N + j, gz = ez * N + k;
+                    int64_t v[3] = {i, j, k}, w[3];
+                    for (int a = 0; a < 3; ++a)
+                        w[a] = flip[o][a] ? N - v[perm[o][a]] : v[perm[o][a]];
+                    int64_t gx = ex * N + w[0], gy = ey * N + w[1], gz = ez * N + w[2];
                     int64_t L = gx + M * (gy + M * gz);
                     int64_t l = s * q * q * q + i + q * (j + q * k);
                     int on_boundary = gx == 0 || gy == 0 || gz == 0 ||

@@ -34,6 +34,7 @@ BS_EALIGN = -5
 SHUFFLE_ELEMS = 1
 PERMUTE_GLOBAL = 2
 MASK_BOUNDARY = 4
+ROTATE_ELEMS = 8
 GATHER_SEG_MAX = 4096
 GATHER_SEG_DEFAULT = 2048
 

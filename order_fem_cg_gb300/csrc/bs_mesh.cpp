@@ -12,8 +12,10 @@
 // Numbering (setup convention of this library, stated in bs.h): lattice
 // element ex + E(ey + E ez); slot s holds lattice element elemPerm[s];
 // local index s (N+1)^3 + i + (N+1)(j + (N+1)k); lattice node
-// (ex N + i, ey N + j, ez N + k), x fastest; global id nodePerm[lattice].
-// Seeded permutations: indices ordered by (SplitMix64 draw, index).
+// (ex N + w0, ey N + w1, ez N + w2), x fastest, where w is (i, j, k) under
+// the element's rotation (the identity unless BS_MESH_ROTATE_ELEMS); global
+// id nodePerm[lattice].  Seeded permutations: indices ordered by
+// (SplitMix64 draw, index); rotations: ((draw >> 11) * 24) >> 53.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -85,6 +87,53 @@ std::vector<int32_t> seeded_permutation(uint64_t seed, uint64_t tag, int64_t n)
     return idx;
 }
 
+// Rotation o of the reference cube as a signed axis permutation: output
+// axis a takes input axis perm[a], reversed if flip[a].  The 24 proper
+// rotations in the library's fixed order: permutations of (0, 1, 2) in
+// lexicographic order, each with the flip masks 0..7 (bit a = axis a)
+// whose matrix has determinant +1; rotation 0 is the identity.
+struct Rotation {
+    int perm[3];
+    bool flip[3];
+};
+
+std::vector<Rotation> cube_rotations()
+{
+    std::vector<Rotation> r;
+    int p[3] = {0, 1, 2};
+    do {
+        // parity of the permutation: count inversions
+        const int inv = (p[0] > p[1]) + (p[0] > p[2]) + (p[1] > p[2]);
+        for (int f = 0; f < 8; ++f) {
+            const int nflip = (f & 1) + ((f >> 1) & 1) + ((f >> 2) & 1);
+            if (((inv + nflip) & 1) != 0)
+                continue;
+            Rotation q;
+            for (int a = 0; a < 3; ++a) {
+                q.perm[a] = p[a];
+                q.flip[a] = ((f >> a) & 1) != 0;
+            }
+            r.push_back(q);
+        }
+    } while (std::next_permutation(p, p + 3));
+    return r;
+}
+
+// Rotation index in [0, 24) of every lattice element, from stream
+// (seed, 10): ((draw >> 11) * 24) >> 53.
+std::vector<uint8_t> seeded_orientations(uint64_t seed, int64_t K)
+{
+    const uint64_t state0 = seed ^ (10ull * kGamma);
+    std::vector<uint8_t> o(K);
+    parallel_for(K, [&](int64_t a, int64_t b) {
+        for (int64_t e = a; e < b; ++e) {
+            const uint64_t z = splitmix_out(state0 + static_cast<uint64_t>(e + 1) * kGamma);
+            o[e] = static_cast<uint8_t>(((z >> 11) * 24u) >> 53);
+        }
+    });
+    return o;
+}
+
 std::vector<int32_t> identity(int64_t n)
 {
     std::vector<int32_t> v(n);
@@ -102,7 +151,7 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
         return BS_EINVAL;
     *out = nullptr;
     if (E < 1 || N < 1 || seg_target < 8 || seg_target > BS_GATHER_SEG_MAX ||
-        (flags & ~7u) != 0)
+        (flags & ~15u) != 0)
         return BS_EINVAL;
     const int64_t q = N + 1, Np = q * q * q, M = static_cast<int64_t>(E) * N + 1;
     const int64_t K = static_cast<int64_t>(E) * E * E;
@@ -127,19 +176,32 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
         const std::vector<int32_t> nodePerm =
             (flags & BS_MESH_PERMUTE_GLOBAL) ? seeded_permutation(seed, 2, NG) : identity(NG);
         const bool mask = (flags & BS_MESH_MASK_BOUNDARY) != 0;
+        const bool rotate = (flags & BS_MESH_ROTATE_ELEMS) != 0;
+        const std::vector<uint8_t> orient =
+            rotate ? seeded_orientations(seed, K) : std::vector<uint8_t>();
+        const std::vector<Rotation> rot = cube_rotations();
+        const int nrot = rotate ? 24 : 1;
 
-        // Lattice offset of each element-local node relative to the element's
-        // lattice corner, and whether it can touch the box boundary per axis.
-        std::vector<int64_t> off(Np);
-        std::vector<int32_t> ni(Np), nj(Np), nk(Np);
-        for (int64_t k = 0, n = 0; k < q; ++k)
-            for (int64_t j = 0; j < q; ++j)
-                for (int64_t i = 0; i < q; ++i, ++n) {
-                    off[n] = i + M * (j + M * k);
-                    ni[n] = static_cast<int32_t>(i);
-                    nj[n] = static_cast<int32_t>(j);
-                    nk[n] = static_cast<int32_t>(k);
-                }
+        // Per rotation: the lattice offset of each element-local node from
+        // the element's lattice corner, and its lattice coordinates in the
+        // element (for the boundary mask).
+        std::vector<int64_t> off(nrot * Np);
+        std::vector<int32_t> ni(nrot * Np), nj(nrot * Np), nk(nrot * Np);
+        for (int o = 0; o < nrot; ++o)
+            for (int64_t k = 0, n = 0; k < q; ++k)
+                for (int64_t j = 0; j < q; ++j)
+                    for (int64_t i = 0; i < q; ++i, ++n) {
+                        const int64_t v[3] = {i, j, k};
+                        int64_t w[3];
+                        for (int a = 0; a < 3; ++a) {
+                            const int64_t c = v[rot[o].perm[a]];
+                            w[a] = rot[o].flip[a] ? N - c : c;
+                        }
+                        off[o * Np + n] = w[0] + M * (w[1] + M * w[2]);
+                        ni[o * Np + n] = static_cast<int32_t>(w[0]);
+                        nj[o * Np + n] = static_cast<int32_t>(w[1]);
+                        nk[o * Np + n] = static_cast<int32_t>(w[2]);
+                    }
 
         m->scatterIds.resize(NL);
         int32_t *ids = m->scatterIds.data();
@@ -148,11 +210,13 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
                 const int64_t e = elemPerm[s];
                 const int64_t ex = e % E, ey = (e / E) % E, ez = e / (static_cast<int64_t>(E) * E);
                 const int64_t base = ex * N + M * (ey * N + M * (ez * N));
+                const int64_t ro = rotate ? orient[e] * Np : 0;
                 int32_t *row = ids + s * Np;
                 for (int64_t n = 0; n < Np; ++n) {
-                    int32_t g = nodePerm[base + off[n]];
+                    int32_t g = nodePerm[base + off[ro + n]];
                     if (mask) {
-                        const int64_t gx = ex * N + ni[n], gy = ey * N + nj[n], gz = ez * N + nk[n];
+                        const int64_t gx = ex * N + ni[ro + n], gy = ey * N + nj[ro + n],
+                                      gz = ez * N + nk[ro + n];
                         if (gx == 0 || gy == 0 || gz == 0 || gx == M - 1 || gy == M - 1 ||
                             gz == M - 1)
                             g = -1;

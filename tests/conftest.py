@@ -29,6 +29,17 @@ def pytest_configure(config):
     build_lib()
 
 
+def oracle_ids(cfg):
+    """The oracle's local-to-global table of a mesh workload, honouring all
+    of its flags (element order, global numbering, mask, orientations)."""
+    import bsinputs as gen
+    import oracle
+    ep, npm = gen.mesh_perms(cfg)
+    orient = gen.element_orientations(cfg) if cfg.flags & gen.ROTATE_ELEMS else None
+    return oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY),
+                                  orient)
+
+
 def read_golden(name):
     """Rows of a golden fixture, comments stripped, as lists of tokens."""
     rows = []

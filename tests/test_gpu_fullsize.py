@@ -15,7 +15,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
-from conftest import build_lib  # noqa: E402
+from conftest import build_lib, oracle_ids  # noqa: E402
 
 build_lib()
 import bench  # noqa: E402
@@ -30,15 +30,17 @@ def close(a, b, rtol=1e-12):
     return abs(a - b) <= rtol * abs(b)
 
 
-@pytest.mark.parametrize("planned", [True, False])
-def test_stress_step_matches_oracle(planned):
-    cfg = gen.WORKLOADS["stress"]
+@pytest.mark.parametrize("name,planned", [("stress", True), ("stress", False),
+                                          ("stress_masked", True)])
+def test_stress_step_matches_oracle(name, planned):
+    """The stress mesh, and the same scale with masked boundary nodes and
+    randomly oriented elements."""
+    cfg = gen.WORKLOADS[name]
     torch.cuda.set_device(0)
     wl = bench.Workload(cfg, torch, bs, torch.device("cuda", 0), planned=planned)
     assert wl.planned == planned
     h, v, sc = wl.h, wl.v, wl.sc
-    ep, npm = gen.mesh_perms(cfg)
-    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm)
+    ids = oracle_ids(cfg)
     assert np.array_equal(wl.mesh.tables()["scatterIds"], ids)
     stream = torch.cuda.current_stream()
     for name in wl.names:

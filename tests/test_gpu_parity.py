@@ -18,7 +18,7 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
-from conftest import build_lib  # noqa: E402
+from conftest import build_lib, oracle_ids  # noqa: E402
 
 build_lib()
 import order_fem_cg_gb300 as bs  # noqa: E402
@@ -161,8 +161,7 @@ def mesh_case(cfg, seg=None, planned=False, sizes=None):
     if sizes is not None:
         assert m.plan(*sizes) == bs.BS_OK
     ids = m.tables()["scatterIds"]
-    ep, npm = gen.mesh_perms(cfg)
-    ids_o = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+    ids_o = oracle_ids(cfg)
     assert np.array_equal(ids, ids_o)
     t = m.to_device(0, planned=planned)
     assert (t.plan is not None) == planned
@@ -178,6 +177,8 @@ MESHES = [
     (gen.MeshConfig("plain", 5, 2, 3, 0), 3000),
     (gen.MeshConfig("one", 1, 1, 5, 3), None),
     (gen.MeshConfig("onemask", 1, 3, 5, 7), 8),
+    (gen.MeshConfig("rot", 5, 3, 31, 11), None),
+    (gen.MeshConfig("rotmask", 4, 5, 32, 15), 1000),
     (gen.WORKLOADS["mid"], None),
 ]
 
@@ -193,6 +194,9 @@ PLANNED = [
     (gen.MeshConfig("masked4", 6, 4, 17, 7), (500, 333, 700, 600, 4)),
     (gen.MeshConfig("one", 1, 1, 5, 3), None),
     (gen.MeshConfig("onemask", 1, 3, 5, 7), (3, 5, 7, 9, 2)),
+    (gen.MeshConfig("rot", 5, 3, 31, 11), None),
+    (gen.MeshConfig("rotmask", 4, 5, 32, 15), (700, 500, 900, 800, 1)),
+    (gen.MeshConfig("midrotmask", 20, 7, 33, 15), None),
     (gen.WORKLOADS["mid"], None),
     (gen.WORKLOADS["mid"], (16384, 24576, 16384, 22528, 2)),
     (gen.WORKLOADS["large"], None),

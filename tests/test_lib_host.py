@@ -9,7 +9,7 @@ import pytest
 
 import bsinputs as gen
 import oracle
-from conftest import ROOT, build_lib
+from conftest import ROOT, build_lib, oracle_ids
 
 
 @pytest.fixture(scope="module")
@@ -50,7 +50,7 @@ def test_mesh_rejects_bad_arguments(bs):
         with pytest.raises(bs.BSError):
             bs.Mesh(E, N, 1, seg_target=seg)
     with pytest.raises(bs.BSError):
-        bs.Mesh(2, 2, 1, flags=8)
+        bs.Mesh(2, 2, 1, flags=16)
 
 
 def _expected_csr(ids, NG):
@@ -62,7 +62,9 @@ def _expected_csr(ids, NG):
 
 
 CASES = [("tiny", None), ("mid", None), ((2, 2, 0), None), ((3, 4, 7), None), ((1, 1, 3), None),
-         ((5, 3, 3), 8), ((4, 2, 7), 100), ((6, 5, 3), 4096)]
+         ((5, 3, 3), 8), ((4, 2, 7), 100), ((6, 5, 3), 4096), ((3, 4, 15), None), ((4, 2, 8), 100),
+         ((5, 5, 11), None), ((2, 7, 12), 8)]
+
 
 
 @pytest.mark.parametrize("which,seg", CASES)
@@ -76,14 +78,14 @@ def test_mesh_builder_matches_oracle(bs, which, seg):
     assert m.validate() == bs.BS_OK
     assert (m.NL, m.NG, m.K) == (cfg.NL, cfg.NG, cfg.K)
     t = m.tables()
-    ep, npm = gen.mesh_perms(cfg)
-    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+    ids = oracle_ids(cfg)
     assert np.array_equal(t["scatterIds"], ids)
     rs, li = _expected_csr(ids, cfg.NG)
     assert np.array_equal(t["rowStarts"], rs)
     assert np.array_equal(t["localIds"], li)
     assert m.nnz == int((ids >= 0).sum())
-    assert m.max_row == (8 if cfg.E >= 2 else 1)
+    masked_small = cfg.flags & gen.MASK_BOUNDARY and cfg.E < 2
+    assert m.max_row == (8 if cfg.E >= 2 else (0 if masked_small else 1))
     bsx = t["blockStarts"]
     assert bsx[0] == 0 and bsx[-1] == cfg.NG and np.all(np.diff(bsx) > 0)
     target = seg or bs.GATHER_SEG_DEFAULT

@@ -40,9 +40,33 @@ def gll_nodes(N):
     return np.concatenate([[-1.0], inner, [1.0]])
 
 
-def local_coords(E, N, elem_perm):
+def cube_rotations():
+    """The 24 proper rotations of the cube in the numbering's order, as
+    (perm, flip): axis permutations in lexicographic order, flip masks
+    0..7 (bit a: output axis a reversed), determinant +1 kept."""
+    import itertools
+    out = []
+    for perm in itertools.permutations(range(3)):
+        inv = sum(perm[a] > perm[b] for a in range(3) for b in range(a + 1, 3))
+        for f in range(8):
+            flip = tuple((f >> a) & 1 for a in range(3))
+            if (inv + sum(flip)) % 2 == 0:
+                out.append((perm, flip))
+    return out
+
+
+def rotation_matrix(perm, flip):
+    """Linear part of the map v -> w, w_a = +-v[perm[a]]."""
+    R = np.zeros((3, 3), dtype=int)
+    for a in range(3):
+        R[a, perm[a]] = -1 if flip[a] else 1
+    return R
+
+
+def local_coords(E, N, elem_perm, orient=None):
     """(x, y, z) of each local node: element lattice cell mapped to [0,1]^3,
-    reference GLL node (r_i, s_j, t_k) mapped affinely into it."""
+    reference GLL node of index w = rotation(i, j, k) mapped affinely into
+    it (orient[e] selects the rotation of lattice element e)."""
     r = gll_nodes(N)
     q = N + 1
     K = E ** 3
@@ -50,17 +74,25 @@ def local_coords(E, N, elem_perm):
     ex, ey, ez = e % E, (e // E) % E, e // (E * E)
     # local node n = i + q (j + q k) inside a slot, i fastest
     n = np.arange(q ** 3)
-    i, j, k = n % q, (n // q) % q, n // (q * q)
-    x = (ex[:, None] + (1.0 + r[i])[None, :] / 2.0) / E
-    y = (ey[:, None] + (1.0 + r[j])[None, :] / 2.0) / E
-    z = (ez[:, None] + (1.0 + r[k])[None, :] / 2.0) / E
+    v = np.stack([n % q, (n // q) % q, n // (q * q)])          # 3 x q^3
+    rots = cube_rotations()
+    o = np.zeros(K, dtype=np.int64) if orient is None else np.asarray(orient)[e].astype(np.int64)
+    w = np.empty((K, 3, q ** 3), dtype=np.int64)
+    for idx, (perm, flip) in enumerate(rots):
+        sel = o == idx
+        if sel.any():
+            wa = np.stack([N - v[perm[a]] if flip[a] else v[perm[a]] for a in range(3)])
+            w[sel] = wa[None]
+    x = (ex[:, None] + (1.0 + r[w[:, 0]]) / 2.0) / E
+    y = (ey[:, None] + (1.0 + r[w[:, 1]]) / 2.0) / E
+    z = (ez[:, None] + (1.0 + r[w[:, 2]]) / 2.0) / E
     return np.stack([x.reshape(-1), y.reshape(-1), z.reshape(-1)], axis=1).reshape(K * q ** 3, 3)
 
 
-def geometric_ids(E, N, elem_perm, node_perm, mask=False):
+def geometric_ids(E, N, elem_perm, node_perm, mask=False, orient=None):
     """Expected local-to-global table from geometry alone: the lattice number
     of a node is its rank along each axis among the distinct coordinates."""
-    c = local_coords(E, N, elem_perm)
+    c = local_coords(E, N, elem_perm, orient)
     M = E * N + 1
     g = []
     for a in range(3):
@@ -75,8 +107,8 @@ def geometric_ids(E, N, elem_perm, node_perm, mask=False):
     return ids
 
 
-def ids_match_geometry(E, N, elem_perm, node_perm, ids, mask=False):
-    c = local_coords(E, N, elem_perm)
+def ids_match_geometry(E, N, elem_perm, node_perm, ids, mask=False, orient=None):
+    c = local_coords(E, N, elem_perm, orient)
     _, inv = np.unique(c, axis=0, return_inverse=True)
     inv = inv.reshape(-1)
     # two local nodes share a global id iff they share a point
@@ -86,7 +118,7 @@ def ids_match_geometry(E, N, elem_perm, node_perm, ids, mask=False):
             return False
         if len(set(g for _, g in pairs)) != len(pairs):
             return False
-    return np.array_equal(np.asarray(ids), geometric_ids(E, N, elem_perm, node_perm, mask))
+    return np.array_equal(np.asarray(ids), geometric_ids(E, N, elem_perm, node_perm, mask, orient))
 
 
 def multiplicity_closed_form(E, N):
@@ -101,7 +133,9 @@ def mesh(cfg_or_EN, seed=12345, flags=gen.SHUFFLE_ELEMS | gen.PERMUTE_GLOBAL):
         E, N = cfg_or_EN
         cfg = gen.MeshConfig("t", E, N, seed, flags)
     ep, npm = gen.mesh_perms(cfg)
-    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY))
+    orient = gen.element_orientations(cfg) if cfg.flags & gen.ROTATE_ELEMS else None
+    ids = oracle.box_scatter_ids(cfg.E, cfg.N, ep, npm, bool(cfg.flags & gen.MASK_BOUNDARY),
+                                 orient)
     return cfg, ep, npm, ids
 
 
@@ -171,6 +205,49 @@ def test_masked_numbering_matches_geometry(E, N):
     # masked globals = the box-boundary lattice nodes
     unmasked_globals = np.unique(ids[ids >= 0])
     assert unmasked_globals.size == max(M - 2, 0) ** 3
+
+
+def test_rotations_form_the_cube_rotation_group():
+    """The numbering's 24 orientations are exactly the rotation group of the
+    cube: orthogonal, determinant +1, distinct, closed under composition,
+    the identity first."""
+    mats = [rotation_matrix(p, f) for p, f in cube_rotations()]
+    assert len(mats) == 24 and np.array_equal(mats[0], np.eye(3, dtype=int))
+    keys = {m.tobytes() for m in mats}
+    assert len(keys) == 24
+    for m in mats:
+        assert np.array_equal(m @ m.T, np.eye(3, dtype=int)) and round(np.linalg.det(m)) == 1
+    for a in mats:
+        for b in mats:
+            assert (a @ b).tobytes() in keys
+
+
+def test_orientation_draws_definition():
+    cfg = gen.MeshConfig("t", 5, 2, 99, gen.ROTATE_ELEMS)
+    o = gen.element_orientations(cfg)
+    z = [int(v) for v in gen.draws(99, gen.TAG_ORIENT, cfg.K)]
+    assert o.tolist() == [((v >> 11) * 24) >> 53 for v in z]
+    assert set(o.tolist()) <= set(range(24)) and len(set(o.tolist())) > 16
+    assert not gen.element_orientations(gen.MeshConfig("t", 5, 2, 99, 3)).any()
+
+
+@pytest.mark.parametrize("E,N,flags", [(2, 2, 8), (3, 3, 11), (2, 5, 15), (1, 4, 8), (3, 2, 12)])
+def test_rotated_numbering_matches_geometry(E, N, flags):
+    """Rotated elements still tile the box: two locals share a global id iff
+    they share a point, and masked ids are exactly the boundary points."""
+    cfg, ep, npm, ids = mesh((E, N), seed=300 + E * 10 + N, flags=flags)
+    orient = gen.element_orientations(cfg)
+    assert ids_match_geometry(E, N, ep, npm, ids, mask=bool(flags & gen.MASK_BOUNDARY),
+                              orient=orient)
+    if E > 1 and N > 1:
+        # the rotations matter: the table differs from the unrotated one
+        plain = oracle.box_scatter_ids(E, N, ep, npm, bool(flags & gen.MASK_BOUNDARY))
+        assert not np.array_equal(ids, plain)
+    m = oracle.gather(ids, (ids >= 0).astype(np.float64), cfg.NG)
+    if not flags & gen.MASK_BOUNDARY:
+        hist = dict(zip(*np.unique(m, return_counts=True)))
+        assert {int(k): int(v) for k, v in hist.items()} == \
+            {k: v for k, v in multiplicity_closed_form(E, N).items() if v}
 
 
 def test_multiplicity_closed_form_golden(golden):
