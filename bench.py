@@ -647,6 +647,7 @@ def run_sweep(args):
                       lambda v, a: bs.bs_cg_update(v[0], v[1], v[2], v[3], alpha=a, rdotr=v[4])),
     }
     res = {k: [] for k in ops}
+    cap = torch.cuda.Stream()
     for log2n in gen.SWEEP_LOG2:
         x, y, alpha = gen.sweep_vectors(log2n)
         n = x.size
@@ -654,6 +655,7 @@ def run_sweep(args):
              torch.from_numpy(x).to(dev), torch.from_numpy(y).to(dev),
              torch.zeros(1, dtype=torch.float64, device=dev)]
         reps = 50 if n <= (1 << 20) else 10
+        K = 100 if n <= (1 << 20) else 10     # launches per stream / graph sample
         for name, (nbytes, fn) in ops.items():
             for _ in range(3):
                 fn(v, alpha)
@@ -668,16 +670,50 @@ def run_sweep(args):
                 torch.cuda.synchronize()
                 host_t.append(time.perf_counter() - t0)
                 dev_t.append(e0.elapsed_time(e1) * 1e-3)
-            res[name].append((n, nbytes(n), statistics.median(host_t), statistics.median(dev_t)))
+            # K back-to-back launches on one stream, device-timed (no host sync
+            # between them): what a pipelined solver pays per operation
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(K):
+                fn(v, alpha)
+            e1.record(stream)
+            e1.synchronize()
+            stream_t = e0.elapsed_time(e1) * 1e-3 / K
+            # the same K launches replayed from one CUDA graph
+            cap.wait_stream(stream)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                for _ in range(K):
+                    fn(v, alpha)
+            g.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            graph_t = e0.elapsed_time(e1) * 1e-3 / K
+            del g
+            res[name].append((n, nbytes(n), statistics.median(host_t), statistics.median(dev_t),
+                              stream_t, graph_t))
         del v
     for name, pts in res.items():
         B = np.array([p[1] for p in pts], dtype=np.float64)
-        T = np.array([p[2] for p in pts])
-        T0, Wmax = pm.fit(B, T)
+        fits = {}
+        for key, col in (("host", 2), ("stream", 4), ("graph", 5)):
+            T0, Wmax = pm.fit(B, np.array([p[col] for p in pts]))
+            fits[key] = {"T0_us": T0 * 1e6, "Wmax_GBs": Wmax / 1e9, "B08_bytes": pm.b_08(T0, Wmax),
+                         "Wmax_frac": Wmax / 1e9 / peak}
+        h = fits["host"]
         line = {"mode": "sweep", "op": name, "timer": "host (launch -> synchronize), median",
-                "T0_us": T0 * 1e6, "Wmax_GBs": Wmax / 1e9, "B08_bytes": pm.b_08(T0, Wmax),
-                "Wmax_frac": Wmax / 1e9 / peak, "peak_GBs": peak, "peak_source": peak_src,
+                "T0_us": h["T0_us"], "Wmax_GBs": h["Wmax_GBs"], "B08_bytes": h["B08_bytes"],
+                "Wmax_frac": h["Wmax_frac"], "peak_GBs": peak, "peak_source": peak_src,
+                "launch_modes": {
+                    "host": "one launch then cudaStreamSynchronize, host clock (the pages' method)",
+                    "stream": "back-to-back launches on one stream, CUDA events, per launch",
+                    "graph": "the same launches replayed from one CUDA graph, CUDA events"},
+                "fits": fits,
                 "points": [{"n": p[0], "bytes": p[1], "host_us": p[2] * 1e6, "event_us": p[3] * 1e6,
+                            "stream_us": p[4] * 1e6, "graph_us": p[5] * 1e6,
                             "GB/s_host": p[1] / p[2] / 1e9, "GB/s_event": p[1] / p[3] / 1e9}
                            for p in pts]}
         print(json.dumps(line), flush=True)

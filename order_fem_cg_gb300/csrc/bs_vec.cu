@@ -127,12 +127,20 @@ __device__ __forceinline__ double block_sum(double v, double *sh)
 }
 
 // Writes this block's partial; the last block to arrive sums all partials
-// in index order and writes the result, then re-arms the counter.
+// in index order and writes the result, then re-arms the counter.  A grid
+// of one block writes its sum directly (as 0.0 + sum: the same bits the
+// finisher's sum from +0.0 gives), saving the fence, the counter round trip
+// and the second block sum -- the launch-latency floor of small reductions.
 __device__ __forceinline__ void finish_reduction(double v, const RedOut &o)
 {
     __shared__ double sh[kThreads / 32];
     __shared__ unsigned int ticket;
     v = block_sum(v, sh);
+    if (gridDim.x == 1) {
+        if (threadIdx.x == 0)
+            *o.out = 0.0 + v;
+        return;
+    }
     if (threadIdx.x == 0) {
         o.partials[blockIdx.x] = v;
         __threadfence();
