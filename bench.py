@@ -803,6 +803,36 @@ def cg_solve_times(cfg, iters, reps, warmup, torch, bs, dev):
             float(rr[-1] / rr[0]))
 
 
+def cg_fused_times(cfg, iters, reps, warmup, torch, bs, dev):
+    """ms per CG iteration of the one-kernel solve (grid barriers), mass
+    operator: a solve of `iters` iterations minus one of 0 iterations."""
+    mesh = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    t = mesh.to_device(0, planned=False)
+    NG = cfg.NG
+    d = torch.from_numpy(gen.mass_diagonal(cfg.E, cfg.N)).to(dev)
+    b = torch.from_numpy(gen.uniform_pm1(cfg.seed, gen.TAG_R, NG)).to(dev)
+    x, r, p, Ap = (torch.zeros(NG, dtype=torch.float64, device=dev) for _ in range(4))
+    pL = torch.zeros(cfg.NL, dtype=torch.float64, device=dev)
+    scal = {k: torch.zeros(2 * k + 1, dtype=torch.float64, device=dev) for k in (0, iters)}
+
+    def timed(k):
+        for _ in range(warmup):
+            bs.bs_cg_solve_fused(t, d, b, x, r, p, Ap, pL, k, scal[k])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            bs.bs_cg_solve_fused(t, d, b, x, r, p, Ap, pL, k, scal[k])
+        e1.record()
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    ms = (timed(iters) - timed(0)) / iters
+    if bs.default_context().device_status() != bs.BS_OK:
+        raise RuntimeError("fused CG solve reported a device error")
+    return ms
+
+
 def run_cg_solve(args):
     import torch
 
@@ -819,6 +849,10 @@ def run_cg_solve(args):
     peak, src = measured_peak()
     tiny = gen.WORKLOADS["tiny"]
     t_eager, t_graph, _ = cg_solve_times(tiny, 50, 20, 3, torch, bs, dev)
+    t_fused = cg_fused_times(tiny, 50, 20, 3, torch, bs, dev)
+    mid = gen.WORKLOADS["mid"]
+    m_eager, m_graph, _ = cg_solve_times(mid, 20, 10, 3, torch, bs, dev)
+    m_fused = cg_fused_times(mid, 20, 10, 3, torch, bs, dev)
     print(json.dumps({
         "mode": "cg_solve", "workload": cfg.name, "operator": "A = Z^T diag(GLL mass) Z",
         "iters": K, "rr_ratio": rr_ratio, "launches_per_iter": 6,
@@ -827,7 +861,11 @@ def run_cg_solve(args):
         "frac": nbytes / (graph * 1e-3) / 1e9 / peak, "peak_source": src,
         "tiny": {"workload": tiny.name, "eager_us_per_iter": 1e3 * t_eager,
                  "graph_us_per_iter": 1e3 * t_graph,
-                 "launch_us_saved_per_kernel": 1e3 * (t_eager - t_graph) / 6}}), flush=True)
+                 "one_kernel_us_per_iter": 1e3 * t_fused,
+                 "launch_us_saved_per_kernel": 1e3 * (t_eager - t_graph) / 6},
+        "mid": {"workload": mid.name, "eager_us_per_iter": 1e3 * m_eager,
+                "graph_us_per_iter": 1e3 * m_graph, "one_kernel_us_per_iter": 1e3 * m_fused}}),
+        flush=True)
     return 0
 
 

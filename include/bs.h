@@ -55,6 +55,7 @@ extern "C" {
 #define BS_ENOMEM (-3)  /* host or context workspace allocation failed             */
 #define BS_EBOUNDS (-4) /* an index table entry is out of range (host or device)    */
 #define BS_EALIGN (-5)  /* reserved; never returned (misalignment is peeled)       */
+#define BS_ETIMEOUT (-6) /* a bounded device-side wait gave up (see bs_ctx_device_status) */
 
 /* ---- mesh flags (bs_mesh_build_box) ------------------------------------- */
 #define BS_MESH_SHUFFLE_ELEMS 1u   /* seeded random order of elements in storage */
@@ -148,8 +149,9 @@ int bs_ctx_destroy(bs_ctx *ctx);
 int bs_ctx_num_sms(const bs_ctx *ctx);
 /* Synchronises `stream`, then reads and clears the device error flag that
  * the gather/scatter kernels raise on an out-of-range table entry (they
- * skip that entry instead of touching memory out of bounds).  *out_status
- * is BS_OK or BS_EBOUNDS. */
+ * skip that entry instead of touching memory out of bounds) and that
+ * bs_cg_solve_fused raises when a grid barrier gives up waiting.
+ * *out_status is BS_OK, BS_EBOUNDS or BS_ETIMEOUT. */
 int bs_ctx_device_status(bs_ctx *ctx, void *stream, int *out_status);
 
 /* ---- BS1-BS5: mesh-free vector operations ---------------------------------
@@ -346,6 +348,30 @@ int bs_cg_iteration(bs_ctx *ctx, const bs_gs_dev *t, const double *pG, double *p
 int bs_cg_solve(bs_ctx *ctx, const bs_gs_dev *t, const double *dL, const double *bG, double *xG,
                 double *rG, double *pG, double *ApG, int32_t iters, double *scal_dev,
                 void *stream);
+
+/* The same iteration as bs_cg_solve (same operations, same order of
+ * arithmetic for every vector entry; the reductions sum in another order)
+ * in ONE cooperative kernel: every block stays resident and the blocks
+ * meet at grid barriers (four per iteration: after the scatter with the
+ * local operator, after the CSR gather with p.Ap summed in the same pass,
+ * after BS5, after the p update), so an iteration costs no launch at all.
+ * For meshes small enough that launches set the time (the one-pass
+ * gather/scatter phases do random 8-byte accesses); no plan is needed.
+ * pL [NL] is caller scratch (q_L).  Each barrier wait is bounded: if one
+ * gives up, the kernel ends early and bs_ctx_device_status reports
+ * BS_ETIMEOUT.  Uses the context's reduction workspace (one call at a time
+ * per context).  BS_ECUDA if the device cannot run the grid cooperatively. */
+int bs_cg_solve_fused(bs_ctx *ctx, const bs_gs_dev *t, const double *dL, const double *bG,
+                      double *xG, double *rG, double *pG, double *ApG, double *pL, int32_t iters,
+                      double *scal_dev, void *stream);
+
+/* Diagnostic of bs_cg_solve_fused's grid barrier: a cooperative grid of one
+ * block per SM meets twice at the barrier.  With absent_block < 0 every
+ * block arrives (bs_ctx_device_status then reports BS_OK); with
+ * absent_block = b, block b leaves without arriving and every other block's
+ * bounded wait runs out (~0.1-0.5 s): the kernel ends and
+ * bs_ctx_device_status reports BS_ETIMEOUT.  Nothing faults or hangs. */
+int bs_probe_grid_barrier(bs_ctx *ctx, int absent_block, void *stream);
 
 /* ---- diagnostics ----------------------------------------------------------
  * Throughput probe of the binary64 fused multiply-add pipe: launches

@@ -30,6 +30,7 @@ BS_ECUDA = -2
 BS_ENOMEM = -3
 BS_EBOUNDS = -4
 BS_EALIGN = -5
+BS_ETIMEOUT = -6
 
 SHUFFLE_ELEMS = 1
 PERMUTE_GLOBAL = 2
@@ -45,7 +46,7 @@ EXPORTS = (
     "bs_mesh_build_box", "bs_mesh_build_box_ex", "bs_mesh_info", "bs_mesh_tables",
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
     "bs_probe_dfma", "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
-    "bs_apply_diag", "bs_axpy_dev", "bs_cg_solve",
+    "bs_apply_diag", "bs_axpy_dev", "bs_cg_solve", "bs_cg_solve_fused", "bs_probe_grid_barrier",
 )
 
 
@@ -124,6 +125,9 @@ def _declare(lib):
         "bs_axpy_dev": ([_vp, _i64, _dbl, _vp, _vp, _vp, _vp, _vp], _int),
         "bs_cg_solve": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 6 + [ctypes.c_int32, _vp, _vp],
                         _int),
+        "bs_cg_solve_fused": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 7 +
+                              [ctypes.c_int32, _vp, _vp], _int),
+        "bs_probe_grid_barrier": ([_vp, _int, _vp], _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
         "bs_mesh_plan": ([_vp] + [ctypes.c_int32] * 5, _int),
@@ -535,6 +539,34 @@ def bs_cg_solve(tables, dL, bG, xG, rG, pG, ApG, iters, scal=None, stream=None, 
         _vec(dL, "dL", tables.NL) if dL is not None else _vp(0), _vec(bG, "bG", NG),
         _vec(xG, "xG", NG), _vec(rG, "rG", NG), _vec(pG, "pG", NG), _vec(ApG, "ApG", NG),
         iters, _vec(scal, "scal", 2 * iters + 1), _stream(stream)), "bs_cg_solve")
+    return scal
+
+
+def bs_probe_grid_barrier(absent_block=-1, stream=None, ctx=None):
+    """Run the fused solve's grid barrier twice; with absent_block >= 0 that
+    block never arrives and the others' bounded waits run out.  Returns the
+    device status (BS_OK or BS_ETIMEOUT)."""
+    ctx = ctx if ctx is not None else default_context()
+    ctx.check(lib.bs_probe_grid_barrier(ctx.handle, int(absent_block), _stream(stream)),
+              "bs_probe_grid_barrier")
+    return ctx.device_status(stream)
+
+
+def bs_cg_solve_fused(tables, dL, bG, xG, rG, pG, ApG, pL, iters, scal=None, stream=None,
+                      ctx=None):
+    """bs_cg_solve's iteration in one cooperative kernel (grid barriers, no
+    launch per iteration) for launch-bound mesh sizes; pL [NL] is scratch."""
+    ctx = _ctx(ctx, bG)
+    NG = tables.NG
+    iters = int(iters)
+    if scal is None:
+        scal = torch.empty(2 * iters + 1, dtype=torch.float64, device=bG.device)
+    ctx.check(lib.bs_cg_solve_fused(
+        ctx.handle, ctypes.byref(tables.struct),
+        _vec(dL, "dL", tables.NL) if dL is not None else _vp(0), _vec(bG, "bG", NG),
+        _vec(xG, "xG", NG), _vec(rG, "rG", NG), _vec(pG, "pG", NG), _vec(ApG, "ApG", NG),
+        _vec(pL, "pL", tables.NL), iters, _vec(scal, "scal", 2 * iters + 1), _stream(stream)),
+        "bs_cg_solve_fused")
     return scal
 
 

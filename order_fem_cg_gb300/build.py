@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libbs.so")
 OBJDIR = os.path.join(ROOT, "_build", "libbs")
 
-SOURCES = ["bs_ctx.cu", "bs_vec.cu", "bs_gs.cu", "bs_gs2.cu", "bs_mesh.cpp", "bs_plan.cpp"]
+SOURCES = ["bs_ctx.cu", "bs_vec.cu", "bs_gs.cu", "bs_gs2.cu", "bs_cg.cu", "bs_mesh.cpp", "bs_plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -39,6 +39,7 @@ extern "C" const char *bs_strerror(int status)
     case BS_ENOMEM: return "out of memory";
     case BS_EBOUNDS: return "index table entry out of range";
     case BS_EALIGN: return "misaligned pointer";
+    case BS_ETIMEOUT: return "a device-side wait timed out";
     default: return "unknown status";
     }
 }
@@ -143,8 +144,10 @@ extern "C" int bs_ctx_device_status(bs_ctx *ctx, void *stream, int *out_status)
     BS_CUDA_TRY(ctx, cudaMemcpyAsync(&flag, ctx->dev_err, sizeof(int), cudaMemcpyDeviceToHost, s));
     BS_CUDA_TRY(ctx, cudaMemsetAsync(ctx->dev_err, 0, sizeof(int), s));
     BS_CUDA_TRY(ctx, cudaStreamSynchronize(s));
-    *out_status = flag ? BS_EBOUNDS : BS_OK;
-    if (flag)
+    *out_status = (flag & BS_DEVERR_TIMEOUT) ? BS_ETIMEOUT : flag ? BS_EBOUNDS : BS_OK;
+    if (flag & BS_DEVERR_TIMEOUT)
+        bs_set_error(ctx, BS_ETIMEOUT, "a grid barrier of a cooperative kernel gave up waiting");
+    else if (flag)
         bs_set_error(ctx, BS_EBOUNDS, "a gather/scatter kernel met an out-of-range table entry");
     return BS_OK;
 }

@@ -37,6 +37,7 @@ struct bs_ctx {
 
 // Bits of the device error flag.
 constexpr int BS_DEVERR_BOUNDS = 1;
+constexpr int BS_DEVERR_TIMEOUT = 2;  // a bounded device-side wait gave up
 
 int bs_set_error(bs_ctx *ctx, int status, const char *fmt, ...);
 

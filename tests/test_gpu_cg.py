@@ -100,12 +100,17 @@ def envelope(ids, dL, b, x0, iters, ref, eta=1e-13):
     return ex, er, err, epap
 
 
-def run(cfg, ids, t, dL, iters, x0):
+def run(cfg, ids, t, dL, iters, x0, fused=False):
     NG = cfg.NG
     b = gen.uniform_pm1(cfg.seed, gen.TAG_R, NG)
     xd, bd = dev(x0), dev(b)
     rd, pd, Apd = (torch.empty(NG, dtype=torch.float64, device=DEV) for _ in range(3))
-    scal = bs.bs_cg_solve(t, dev(dL) if dL is not None else None, bd, xd, rd, pd, Apd, iters)
+    dLd = dev(dL) if dL is not None else None
+    if fused:
+        pL = torch.empty(cfg.NL, dtype=torch.float64, device=DEV)
+        scal = bs.bs_cg_solve_fused(t, dLd, bd, xd, rd, pd, Apd, pL, iters)
+    else:
+        scal = bs.bs_cg_solve(t, dLd, bd, xd, rd, pd, Apd, iters)
     ref = oracle.cg_solve(ids, dL, b, x0, iters)
     ex, er, err, epap = envelope(ids, dL, b, x0, iters, ref)
     s = host(scal)
@@ -146,6 +151,16 @@ def test_cg_solve_matches_oracle(cfg, op, iters, nonzero_x0):
     run(cfg, ids, t, dL, iters, x0)
 
 
+@pytest.mark.parametrize("cfg,op,iters,nonzero_x0", CASES,
+                         ids=lambda v: getattr(v, "name", str(v)))
+def test_cg_solve_fused_matches_oracle(cfg, op, iters, nonzero_x0):
+    """The one-kernel solve (grid barriers) against the same oracle and bounds."""
+    t, ids = mesh(cfg)
+    dL = gen.mass_diagonal(cfg.E, cfg.N) if op == "mass" else None
+    x0 = gen.uniform_pm1(cfg.seed, gen.TAG_X, cfg.NG) if nonzero_x0 else np.zeros(cfg.NG)
+    run(cfg, ids, t, dL, iters, x0, fused=True)
+
+
 @pytest.mark.parametrize("cfg,op,distinct", [(gen.WORKLOADS["tiny"], "identity", 4),
                                              (gen.WORKLOADS["tiny"], "mass", 10)],
                          ids=lambda v: getattr(v, "name", str(v)))
@@ -160,12 +175,18 @@ def test_cg_solve_reaches_the_exact_solution(cfg, op, distinct):
     b = gen.uniform_pm1(cfg.seed, gen.TAG_R, NG)
     xd = torch.zeros(NG, dtype=torch.float64, device=DEV)
     rd, pd, Apd = (torch.empty(NG, dtype=torch.float64, device=DEV) for _ in range(3))
-    scal = host(bs.bs_cg_solve(t, dev(dL) if op == "mass" else None, dev(b), xd, rd, pd, Apd,
-                               distinct + 2))
     xs = b / diag
-    assert np.max(np.abs(host(xd) - xs)) <= 1e-7 * np.max(np.abs(xs))
-    assert scal[distinct + 2] < 1e-8 * scal[0]
-    assert bs.default_context().device_status() == bs.BS_OK
+    for fused in (False, True):
+        xd.zero_()
+        dLd = dev(dL) if op == "mass" else None
+        if fused:
+            pL = torch.empty(cfg.NL, dtype=torch.float64, device=DEV)
+            scal = host(bs.bs_cg_solve_fused(t, dLd, dev(b), xd, rd, pd, Apd, pL, distinct + 2))
+        else:
+            scal = host(bs.bs_cg_solve(t, dLd, dev(b), xd, rd, pd, Apd, distinct + 2))
+        assert np.max(np.abs(host(xd) - xs)) <= 1e-7 * np.max(np.abs(xs)), fused
+        assert scal[distinct + 2] < 1e-8 * scal[0], fused
+        assert bs.default_context().device_status() == bs.BS_OK
 
 
 def test_cg_solve_graph_replay_is_bitwise_eager():
@@ -228,3 +249,15 @@ def test_cg_solve_rejects_bad_arguments():
         bs.bs_cg_solve(t, None, v[0], v[1], v[2], v[3], big[:NG], 2, scal=big[NG - 1:NG + 4])
     with pytest.raises(ValueError):
         bs.bs_cg_solve(t, None, v[0], v[1], v[2], v[3], v[4], 2, scal=v[4][:3])
+
+
+def test_grid_barrier_wait_is_bounded():
+    """The fused solve's grid barrier: with every block present it passes;
+    with one block absent the others' bounded waits run out, the kernel
+    ends, the status says so, and the context keeps working."""
+    assert bs.bs_probe_grid_barrier(-1) == bs.BS_OK
+    assert bs.bs_probe_grid_barrier(3) == bs.BS_ETIMEOUT
+    assert bs.default_context().device_status() == bs.BS_OK     # read and cleared
+    assert bs.bs_probe_grid_barrier(-1) == bs.BS_OK
+    x = dev(np.arange(5.0))
+    assert host(bs.bs_dot(x, x))[0] == 30.0
