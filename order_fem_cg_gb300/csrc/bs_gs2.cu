@@ -21,6 +21,9 @@
 //     coalesced.
 //
 // Global traffic is about twice the algorithmic bytes, all of it in runs.
+// The same request rate bounds these passes: pass 1 writes runs of ~10-18
+// values, so a warp's 32 stores cost ~5 line requests instead of 2, and
+// runs grow only with tile x bucket, which one SM's shared memory caps.
 // One 1024-thread block per SM, up to 227 KB of dynamic shared memory.
 // Every table-derived index is checked; a bad one is skipped and raises the
 // context's device error flag.
