@@ -204,6 +204,16 @@ def mesh_perms(cfg: MeshConfig):
     return ep, npm
 
 
+def random_scatter_ids(seed: int, tag: int, NL: int, NG: int, masked_per_256: int = 0) -> np.ndarray:
+    """An unstructured local-to-global table (int32): local l maps to global
+    ((z_l >> 11) mod NG), or -1 (masked) where (z_l & 255) < masked_per_256.
+    Row lengths (copies per global node) are then about Poisson(NL / NG)."""
+    z = draws(seed, tag, NL)
+    ids = ((z >> np.uint64(11)) % np.uint64(max(NG, 1))).astype(np.int64)
+    ids[(z & np.uint64(255)) < np.uint64(masked_per_256)] = -1
+    return ids.astype(np.int32)
+
+
 def element_orientations(cfg: MeshConfig) -> np.ndarray:
     """Orientation index in [0, 24) of every lattice element (uint8), drawn
     as ((z_e >> 11) * 24) >> 53 from stream (seed, TAG_ORIENT); zeros when

@@ -226,6 +226,18 @@ int bs_mesh_build_box(int E, int N, uint64_t seed, uint32_t flags, bs_mesh **out
  * and seg_target >= 8 (the largest row). */
 int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags, int32_t seg_target,
                          bs_mesh **out);
+/* The same tables (CSR of Z^T, row segments, default two-pass plan) for any
+ * mesh, from the caller's local-to-global table: scatterIds[NL] (host,
+ * copied) with every entry in [-1, NG), -1 = masked local ("GPU accelerated
+ * spectral finite elements on all-hex meshes": I_{l->g}; any element shapes,
+ * orientations and numbering).  Rows (the local copies of a global node) may
+ * have up to BS_GATHER_SEG_MAX entries; the two-pass plan needs at most 32
+ * (else it is left invalid and the one-pass kernels serve).  8 <= seg_target
+ * <= BS_GATHER_SEG_MAX.  The mesh info reports E = N = K = 0, flags = 0.
+ * BS_EBOUNDS for an entry outside [-1, NG), BS_EINVAL for bad sizes or a row
+ * longer than BS_GATHER_SEG_MAX. */
+int bs_mesh_from_ids(int64_t NL, int64_t NG, const int32_t *scatterIds, int32_t seg_target,
+                     bs_mesh **out);
 int bs_mesh_info(const bs_mesh *mesh, bs_mesh_info_t *out);
 /* Host views of the four tables, owned by the mesh (valid until destroy).
  * Any output pointer may be NULL. */

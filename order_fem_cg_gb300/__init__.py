@@ -47,6 +47,7 @@ EXPORTS = (
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
     "bs_probe_dfma", "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
     "bs_apply_diag", "bs_axpy_dev", "bs_cg_solve", "bs_cg_solve_fused", "bs_probe_grid_barrier",
+    "bs_mesh_from_ids",
 )
 
 
@@ -128,6 +129,7 @@ def _declare(lib):
         "bs_cg_solve_fused": ([_vp, ctypes.POINTER(GSDev)] + [_vp] * 7 +
                               [ctypes.c_int32, _vp, _vp], _int),
         "bs_probe_grid_barrier": ([_vp, _int, _vp], _int),
+        "bs_mesh_from_ids": ([_i64, _i64, _vp, ctypes.c_int32, ctypes.POINTER(_vp)], _int),
         "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
         "bs_mesh_plan": ([_vp] + [ctypes.c_int32] * 5, _int),
@@ -328,7 +330,8 @@ def bs_probe_dfma(blocks_per_sm, iters, sink, stream=None, ctx=None):
 # ------------------------------------------------------------- mesh
 
 class Mesh:
-    """Box hex mesh and its index tables, built on the host (bs_mesh_*)."""
+    """Mesh index tables built on the host (bs_mesh_*): a box hex mesh, or
+    any mesh given by its local-to-global table (Mesh.from_ids)."""
 
     def __init__(self, E, N, seed, flags=SHUFFLE_ELEMS | PERMUTE_GLOBAL, seg_target=None):
         h = _vp()
@@ -339,10 +342,27 @@ class Mesh:
                                           ctypes.byref(h))
         if st != BS_OK:
             raise BSError(st, f"bs_mesh_build_box(E={E}, N={N})")
+        self._adopt(h)
+
+    def _adopt(self, h):
         self.handle = h
         info = MeshInfo()
         lib.bs_mesh_info(h, ctypes.byref(info))
         self.info = info
+
+    @classmethod
+    def from_ids(cls, scatter_ids, NG, seg_target=None):
+        """Tables of any mesh from its local-to-global table (int32, -1 =
+        masked, entries < NG)."""
+        ids = np.ascontiguousarray(scatter_ids, dtype=np.int32)
+        h = _vp()
+        st = lib.bs_mesh_from_ids(ids.size, int(NG), ids.ctypes.data,
+                                  int(seg_target or GATHER_SEG_DEFAULT), ctypes.byref(h))
+        if st != BS_OK:
+            raise BSError(st, f"bs_mesh_from_ids(NL={ids.size}, NG={NG})")
+        self = cls.__new__(cls)
+        self._adopt(h)
+        return self
 
     def __del__(self):
         if getattr(self, "handle", None):

@@ -142,6 +142,59 @@ std::vector<int32_t> identity(int64_t n)
     return v;
 }
 
+// From m->scatterIds (N_L entries in [-1, N_G)): the CSR of Z^T (rows in
+// global-id order, local ids ascending per row), the row segments and the
+// default two-pass plan.  Throws std::bad_alloc.
+void finish_tables(bs_mesh *m)
+{
+    const int64_t NL = m->NL, NG = m->NG;
+    const int64_t seg_target = m->seg_target;
+    const int32_t *ids = m->scatterIds.data();
+    m->rowStarts.assign(NG + 1, 0);
+    int32_t *rs = m->rowStarts.data();
+    for (int64_t l = 0; l < NL; ++l)
+        if (ids[l] >= 0)
+            ++rs[ids[l] + 1];
+    int32_t max_row = 0;
+    for (int64_t g = 0; g < NG; ++g) {
+        max_row = std::max(max_row, rs[g + 1]);
+        rs[g + 1] += rs[g];
+    }
+    m->max_row = max_row;
+    m->nnz = rs[NG];
+    m->localIds.resize(m->nnz);
+    {
+        std::vector<int32_t> pos(rs, rs + NG);
+        for (int64_t l = 0; l < NL; ++l)
+            if (ids[l] >= 0)
+                m->localIds[pos[ids[l]]++] = static_cast<int32_t>(l);
+    }
+
+    // Row segments: consecutive rows, at most seg_target entries and at
+    // most seg_target rows each.  seg_max = the largest of any segment's
+    // entry and row counts: the shared-memory staging capacity needed.
+    m->blockStarts.clear();
+    m->blockStarts.push_back(0);
+    int64_t ce = 0, cr = 0;
+    int32_t seg_max = 0;
+    for (int64_t g = 0; g < NG; ++g) {
+        const int64_t len = rs[g + 1] - rs[g];
+        if (cr > 0 && (ce + len > seg_target || cr + 1 > seg_target)) {
+            m->blockStarts.push_back(static_cast<int32_t>(g));
+            seg_max = std::max<int32_t>(seg_max, static_cast<int32_t>(std::max(ce, cr)));
+            ce = 0;
+            cr = 0;
+        }
+        ce += len;
+        cr += 1;
+    }
+    seg_max = std::max<int32_t>(seg_max, static_cast<int32_t>(std::max(ce, cr)));
+    m->blockStarts.push_back(static_cast<int32_t>(NG));
+    m->seg_max = std::max<int32_t>(seg_max, 1);
+    bs_plan_build(m, BS_TILE_S_ROWS, BS_TILE_S_BUCKET, BS_TILE_G_LOCALS, BS_TILE_G_BUCKET,
+                  BS_TILE_CLUSTER);
+}
+
 } // namespace
 
 extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
@@ -226,50 +279,7 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
             }
         });
 
-        // CSR of Z^T: rows in global-id order, local ids ascending per row.
-        m->rowStarts.assign(NG + 1, 0);
-        int32_t *rs = m->rowStarts.data();
-        for (int64_t l = 0; l < NL; ++l)
-            if (ids[l] >= 0)
-                ++rs[ids[l] + 1];
-        int32_t max_row = 0;
-        for (int64_t g = 0; g < NG; ++g) {
-            max_row = std::max(max_row, rs[g + 1]);
-            rs[g + 1] += rs[g];
-        }
-        m->max_row = max_row;
-        m->nnz = rs[NG];
-        m->localIds.resize(m->nnz);
-        {
-            std::vector<int32_t> pos(rs, rs + NG);
-            for (int64_t l = 0; l < NL; ++l)
-                if (ids[l] >= 0)
-                    m->localIds[pos[ids[l]]++] = static_cast<int32_t>(l);
-        }
-
-        // Row segments: consecutive rows, at most seg_target entries and at
-        // most seg_target rows each.  seg_max = the largest of any segment's
-        // entry and row counts: the shared-memory staging capacity needed.
-        m->blockStarts.clear();
-        m->blockStarts.push_back(0);
-        int64_t ce = 0, cr = 0;
-        int32_t seg_max = 0;
-        for (int64_t g = 0; g < NG; ++g) {
-            const int64_t len = rs[g + 1] - rs[g];
-            if (cr > 0 && (ce + len > seg_target || cr + 1 > seg_target)) {
-                m->blockStarts.push_back(static_cast<int32_t>(g));
-                seg_max = std::max<int32_t>(seg_max, static_cast<int32_t>(std::max(ce, cr)));
-                ce = 0;
-                cr = 0;
-            }
-            ce += len;
-            cr += 1;
-        }
-        seg_max = std::max<int32_t>(seg_max, static_cast<int32_t>(std::max(ce, cr)));
-        m->blockStarts.push_back(static_cast<int32_t>(NG));
-        m->seg_max = std::max<int32_t>(seg_max, 1);
-        bs_plan_build(m, BS_TILE_S_ROWS, BS_TILE_S_BUCKET, BS_TILE_G_LOCALS, BS_TILE_G_BUCKET,
-                      BS_TILE_CLUSTER);
+        finish_tables(m);
     } catch (const std::bad_alloc &) {
         delete m;
         return BS_ENOMEM;
@@ -281,6 +291,40 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
 extern "C" int bs_mesh_build_box(int E, int N, uint64_t seed, uint32_t flags, bs_mesh **out)
 {
     return bs_mesh_build_box_ex(E, N, seed, flags, BS_GATHER_SEG_DEFAULT, out);
+}
+
+extern "C" int bs_mesh_from_ids(int64_t NL, int64_t NG, const int32_t *scatterIds,
+                                int32_t seg_target, bs_mesh **out)
+{
+    if (!out)
+        return BS_EINVAL;
+    *out = nullptr;
+    if (NL < 0 || NG < 0 || NL > INT32_MAX || NG >= INT32_MAX || (NL > 0 && !scatterIds) ||
+        seg_target < 8 || seg_target > BS_GATHER_SEG_MAX)
+        return BS_EINVAL;
+    // every entry in [-1, N_G) (-1 = masked local)
+    for (int64_t l = 0; l < NL; ++l)
+        if (scatterIds[l] < -1 || scatterIds[l] >= NG)
+            return BS_EBOUNDS;
+    bs_mesh *m = new (std::nothrow) bs_mesh();
+    if (!m)
+        return BS_ENOMEM;
+    try {
+        m->seg_target = seg_target;
+        m->NL = NL;
+        m->NG = NG;
+        m->scatterIds.assign(scatterIds, scatterIds + NL);
+        finish_tables(m);
+    } catch (const std::bad_alloc &) {
+        delete m;
+        return BS_ENOMEM;
+    }
+    if (m->seg_max > BS_GATHER_SEG_MAX) {  // a row longer than the gather's staging
+        delete m;
+        return BS_EINVAL;
+    }
+    *out = m;
+    return BS_OK;
 }
 
 extern "C" int bs_mesh_info(const bs_mesh *m, bs_mesh_info_t *out)

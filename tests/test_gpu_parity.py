@@ -6,6 +6,8 @@ of the oracle's Dot2 value (the reductions sum in a different order), and
 every reduction is bitwise reproducible run to run.
 """
 
+import types
+
 import numpy as np
 import pytest
 
@@ -223,6 +225,28 @@ def check_scatter_gather(cfg, m, t, ids):
     bs.bs_gather(t, dev(qL), qGd)
     assert bits_equal(host(qGd), oracle.gather(ids, qL, cfg.NG))
     assert bs.default_context().device_status() == bs.BS_OK
+
+
+@pytest.mark.parametrize("NL,NG,masked,planned", [
+    (20000, 4000, 40, False), (20000, 4000, 40, True), (300000, 120000, 0, True),
+    (3000, 100, 0, False), (3000, 100, 0, True), (2000000, 400000, 25, True),
+    (20000, 600, 0, False)])
+def test_scatter_gather_random_tables(NL, NG, masked, planned):
+    """Any local-to-global map (bs_mesh_from_ids): rows of Poisson length,
+    masked locals, empty rows; rows longer than 32 (NL/NG = 33) leave the
+    plan invalid and use the one-pass kernels."""
+    ids = gen.random_scatter_ids(NL + NG, 3, NL, NG, masked)
+    m = bs.Mesh.from_ids(ids, NG)
+    assert m.validate() == bs.BS_OK
+    t = m.to_device(0, planned=planned and m.plan_info().valid)
+    cfg = types.SimpleNamespace(NL=NL, NG=NG, seed=NL)
+    check_scatter_gather(cfg, m, t, ids)
+    if planned and m.plan_info().valid:
+        dL = gen.uniform_range(7, 1, NL, 0.5, 1.5)
+        x = gen.uniform_pm1(7, 2, NG)
+        y = torch.empty(NG, dtype=torch.float64, device=DEV)
+        bs.bs_apply_diag(t, dev(x), dev(dL), y)
+        assert bits_equal(host(y), oracle.apply_diag(ids, dL, x))
 
 
 @pytest.mark.parametrize("planned", [False, True])

@@ -3,6 +3,7 @@
 import os
 import re
 import subprocess
+import types
 
 import numpy as np
 import pytest
@@ -96,6 +97,40 @@ def test_mesh_builder_matches_oracle(bs, which, seg):
     # greedy: a segment ends only when the next row would overflow it
     nxt = rs[np.minimum(bsx[1:-1] + 1, cfg.NG)] - rs[bsx[1:-1]]
     assert np.all((ent[:-1] + nxt > target) | (rows[:-1] + 1 > target))
+
+
+RANDOM_TABLES = [(5000, 1000, 0), (20000, 4000, 40), (3000, 100, 0), (1, 5, 0), (64, 64, 255),
+                 (30000, 25000, 10)]
+
+
+@pytest.mark.parametrize("NL,NG,masked", RANDOM_TABLES)
+def test_mesh_from_ids_matches_numpy(bs, NL, NG, masked):
+    """Tables of an arbitrary (unstructured) local-to-global map."""
+    ids = gen.random_scatter_ids(NL + NG, 1, NL, NG, masked)
+    m = bs.Mesh.from_ids(ids, NG)
+    assert m.validate() == bs.BS_OK
+    assert (m.NL, m.NG, m.E, m.N) == (NL, NG, 0, 0)
+    t = m.tables()
+    assert np.array_equal(t["scatterIds"], ids)
+    rs, li = _expected_csr(ids, NG)
+    assert np.array_equal(t["rowStarts"], rs) and np.array_equal(t["localIds"], li)
+    assert m.nnz == int((ids >= 0).sum())
+    lens = np.diff(rs)
+    assert m.max_row == (int(lens.max()) if NG else 0)
+    assert m.plan_info().valid == (m.max_row <= 32)
+
+
+def test_mesh_from_ids_rejects_bad_tables(bs):
+    with pytest.raises(bs.BSError) as e:
+        bs.Mesh.from_ids(np.array([0, 5, 1], dtype=np.int32), 5)      # 5 >= NG
+    assert e.value.status == bs.BS_EBOUNDS
+    with pytest.raises(bs.BSError):
+        bs.Mesh.from_ids(np.array([0, -2], dtype=np.int32), 3)        # below -1
+    with pytest.raises(bs.BSError) as e:
+        bs.Mesh.from_ids(np.zeros(5000, dtype=np.int32), 2)          # a row of 5000 > 4096
+    assert e.value.status == bs.BS_EINVAL
+    m = bs.Mesh.from_ids(np.zeros(40, dtype=np.int32), 3)             # 40 > 32: no plan
+    assert m.validate() == bs.BS_OK and not m.plan_info().valid
 
 
 def test_masked_mesh_builder_matches_oracle(bs):
@@ -218,14 +253,22 @@ PLAN_CASES = [("tiny", None), ("tiny", (100, 64, 200, 150, 1)), ("tiny", (100, 6
               ((5, 3, 7), (300, 256, 500, 333, 2)), ((3, 4, 3), None), ((2, 2, 7), (4, 3, 5, 8, 4))]
 
 
-@pytest.mark.parametrize("which,sizes", PLAN_CASES)
+@pytest.mark.parametrize("which,sizes", PLAN_CASES + [
+    (("ids", 20000, 4000, 40), None), (("ids", 20000, 4000, 40), (300, 257, 500, 400, 1)),
+    (("ids", 9000, 800, 0), (64, 100, 80, 90, 2)), (("ids", 30000, 25000, 10), None)])
 def test_two_pass_plan_reproduces_oracle(bs, which, sizes):
-    if isinstance(which, str):
+    if isinstance(which, tuple) and which[0] == "ids":
+        _, NL, NG, masked = which
+        ids = gen.random_scatter_ids(NL + NG, 1, NL, NG, masked)
+        m = bs.Mesh.from_ids(ids, NG)
+        cfg = types.SimpleNamespace(NL=NL, NG=NG, seed=NL + NG)
+    elif isinstance(which, str):
         cfg = gen.WORKLOADS[which]
+        m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
     else:
         E, N, flags = which
         cfg = gen.MeshConfig("t", E, N, 0x51 + E, flags)
-    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+        m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
     if sizes is not None:
         assert m.plan(*sizes) == bs.BS_OK
     pi = m.plan_info()
