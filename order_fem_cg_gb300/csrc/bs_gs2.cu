@@ -136,6 +136,37 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar)
     return false;
 }
 
+// Waits for a bulk staging started by stage_start: thread 0 polls the
+// barrier (bounded) while the other threads wait at the block barrier, so
+// the wait issues almost no instructions; a wait that ran out is followed
+// by one more bounded wait for the copy still in flight.  Afterwards every
+// thread tests the (completed) phase once, which is its own acquire of the
+// copied data.  Returns the outcome in every thread.
+__device__ __forceinline__ bool stage_wait(bool bulk, uint64_t *bar)
+{
+    __shared__ int s_staged;
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        if (bulk && !mbar_wait(bar)) {
+            ok = 0;
+            mbar_wait(bar);
+        }
+        s_staged = ok;
+    }
+    __syncthreads();
+    if (bulk && s_staged) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(smem_u32(bar))
+                     : "memory");
+        (void)done;
+    }
+    return s_staged != 0;
+}
+
 // Asks the bulk-copy engine to bring [p, p + bytes) into L2 (no data to the
 // SM, no completion to wait for).  Only whole 16-byte units inside the
 // range are requested, so nothing outside it is touched.
@@ -505,8 +536,13 @@ __device__ __forceinline__ bool emit_runs(const int64_t *runs, const int32_t *ru
                 } else {
                     bad = true;
                 }
-                const int64_t d = static_cast<int64_t>(runD[min(max(c, 0), nne - 1)]) + k;
-                if (d >= 0 && d < nwork)
+                // 32-bit unsigned arithmetic: positions are below nnz < 2^31,
+                // and a corrupted table can only yield d >= nwork (skipped)
+                const uint32_t ci = static_cast<uint32_t>(c);
+                bad |= ci >= static_cast<uint32_t>(nne);
+                const uint32_t d = static_cast<uint32_t>(runD[ci < static_cast<uint32_t>(nne) ? ci : 0u]) +
+                                   static_cast<uint32_t>(k);
+                if (d < static_cast<uint32_t>(nwork))
                     work[d] = v;
                 else
                     bad = true;
@@ -643,10 +679,7 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
         stage(vals, qG + r0 + m0, m1 - m0);
     ok = commit_runs(rf, a.s_runStart, t, a.s_nbuckets, a.nnz, runs, runD) && ok &&
          run_off(runs[a.s_nbuckets]) == e1 - e0;
-    if (bulk && !mbar_wait(&bar)) {
-        ok = false;
-        mbar_wait(&bar);
-    }
+    ok = stage_wait(bulk, &bar) && ok;
     double *tile[CS];
     map_cluster<CS>(vals, tile);
     cluster_barrier<CS>();  // every block's slice is staged
@@ -755,10 +788,7 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
         stage(vals, qL + l0 + m0, m1 - m0);
     ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
          run_off(runs[a.g_nbuckets]) == s1 - s0;
-    if (bulk && !mbar_wait(&bar)) {
-        ok = false;
-        mbar_wait(&bar);
-    }
+    ok = stage_wait(bulk, &bar) && ok;
     double *tile[CS];
     map_cluster<CS>(vals, tile);
     cluster_barrier<CS>();
