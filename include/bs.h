@@ -57,6 +57,15 @@ extern "C" {
 #define BS_EALIGN (-5)  /* reserved; never returned (misalignment is peeled)       */
 #define BS_ETIMEOUT (-6) /* a bounded device-side wait gave up (see bs_ctx_device_status) */
 
+/* Host-side fault injection, to test a caller's error handling without
+ * faulting a GPU: the environment variable BS_FAULT holds a comma-separated
+ * list of "alloc" (bs_ctx_create reports BS_ENOMEM), "launch" (every call
+ * that would launch work reports BS_ECUDA and launches nothing) and
+ * "badtable" (the mesh builders corrupt one scatterIds and one localIds
+ * entry after building: bs_mesh_validate reports BS_EBOUNDS, and the
+ * one-pass kernels skip the entries and raise the device flag).  Read at
+ * every call; unset means no faults. */
+
 /* ---- mesh flags (bs_mesh_build_box) ------------------------------------- */
 #define BS_MESH_SHUFFLE_ELEMS 1u   /* seeded random order of elements in storage */
 #define BS_MESH_PERMUTE_GLOBAL 2u  /* seeded random global node numbering        */

@@ -6,6 +6,7 @@
 #include <new>
 
 #include "bs_internal.h"
+#include "bs_mesh_impl.h"
 
 int bs_set_error(bs_ctx *ctx, int status, const char *fmt, ...)
 {
@@ -18,8 +19,28 @@ int bs_set_error(bs_ctx *ctx, int status, const char *fmt, ...)
     return status;
 }
 
-int bs_check_device(bs_ctx *ctx)
+bool bs_fault(const char *what)
 {
+    const char *s = std::getenv("BS_FAULT");
+    if (!s || !*what)
+        return false;
+    const size_t n = std::strlen(what);
+    while (*s) {
+        const char *e = std::strchr(s, ',');
+        const size_t len = e ? static_cast<size_t>(e - s) : std::strlen(s);
+        if (len == n && std::strncmp(s, what, n) == 0)
+            return true;
+        if (!e)
+            break;
+        s = e + 1;
+    }
+    return false;
+}
+
+int bs_check_device(bs_ctx *ctx, bool launching)
+{
+    if (launching && bs_fault("launch"))
+        return bs_set_error(ctx, BS_ECUDA, "injected launch failure (BS_FAULT=launch)");
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -63,6 +84,8 @@ extern "C" int bs_ctx_create(int device, bs_ctx **out)
     if (!out)
         return BS_EINVAL;
     *out = nullptr;
+    if (bs_fault("alloc"))
+        return BS_ENOMEM;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
         cudaGetLastError();
@@ -137,7 +160,7 @@ extern "C" int bs_ctx_device_status(bs_ctx *ctx, void *stream, int *out_status)
 {
     if (!ctx || !out_status)
         return BS_EINVAL;
-    if (int st = bs_check_device(ctx))
+    if (int st = bs_check_device(ctx, false))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int flag = 0;

@@ -42,7 +42,9 @@ constexpr int BS_DEVERR_TIMEOUT = 2;  // a bounded device-side wait gave up
 int bs_set_error(bs_ctx *ctx, int status, const char *fmt, ...);
 
 // Returns BS_OK if the calling thread's current device is the context's.
-int bs_check_device(bs_ctx *ctx);
+// With launching (every call that launches work), an injected "launch"
+// fault (bs_fault) makes it report BS_ECUDA instead, so nothing launches.
+int bs_check_device(bs_ctx *ctx, bool launching = true);
 
 #define BS_CUDA_TRY(ctx, call)                                                                   \
     do {                                                                                         \

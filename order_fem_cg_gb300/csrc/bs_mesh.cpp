@@ -195,6 +195,18 @@ void finish_tables(bs_mesh *m)
                   BS_TILE_CLUSTER);
 }
 
+// BS_FAULT=badtable: one out-of-range entry in each of scatterIds and
+// localIds (the plan, built before, stays consistent).
+void inject_bad_table(bs_mesh *m)
+{
+    if (!bs_fault("badtable"))
+        return;
+    if (m->NL > 0)
+        m->scatterIds[m->NL / 2] = static_cast<int32_t>(m->NG);
+    if (m->nnz > 0)
+        m->localIds[m->nnz / 2] = static_cast<int32_t>(m->NL);
+}
+
 } // namespace
 
 extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
@@ -284,6 +296,7 @@ extern "C" int bs_mesh_build_box_ex(int E, int N, uint64_t seed, uint32_t flags,
         delete m;
         return BS_ENOMEM;
     }
+    inject_bad_table(m);
     *out = m;
     return BS_OK;
 }
@@ -323,6 +336,7 @@ extern "C" int bs_mesh_from_ids(int64_t NL, int64_t NG, const int32_t *scatterId
         delete m;
         return BS_EINVAL;
     }
+    inject_bad_table(m);
     *out = m;
     return BS_OK;
 }

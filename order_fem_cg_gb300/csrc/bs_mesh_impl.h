@@ -83,6 +83,16 @@ int64_t bs_plan_smem_s1(const bs_plan &p);
 int64_t bs_plan_smem_s2(const bs_plan &p);
 int64_t bs_plan_smem_g1(const bs_plan &p);
 int64_t bs_plan_smem_g2(const bs_plan &p);
+// Host-side fault injection, for tests of a caller's error handling: the
+// comma-separated names in the environment variable BS_FAULT select the
+// failures to fake -- "alloc": bs_ctx_create reports BS_ENOMEM before
+// touching the device; "launch": every launching call reports BS_ECUDA
+// without launching; "badtable": the mesh builders corrupt one scatterIds
+// and one localIds entry (out of range) after building.  Nothing of this
+// faults a GPU; the device kernels' own bounds checks turn a bad table into
+// BS_EBOUNDS.  Reads the environment at every call.
+bool bs_fault(const char *what);
+
 // Marks the first slot of a run in s_src / g_src (tile offsets are < 2^15).
 constexpr uint32_t BS_PLAN_RUN_START = 0x8000u;
 

@@ -470,3 +470,29 @@ def test_apply_diag_rejects_unfusable_plans():
     m, t, ids = mesh_case(cfg, planned=False)
     with pytest.raises(bs.BSError):
         bs.bs_apply_diag(t, x, d, dev(np.zeros(cfg.NG)))
+
+
+def test_injected_faults_are_reported(monkeypatch):
+    """BS_FAULT=launch: calls report BS_ECUDA and launch nothing; a mesh built
+    under BS_FAULT=badtable has out-of-range entries, which the one-pass
+    kernels skip and report.  The context keeps working afterwards."""
+    x, y = dev(np.arange(8.0)), dev(np.zeros(8))
+    monkeypatch.setenv("BS_FAULT", "launch")
+    with pytest.raises(bs.BSError) as e:
+        bs.bs_copy(x, y)
+    assert e.value.status == bs.BS_ECUDA
+    assert bs.default_context().device_status() == bs.BS_OK
+    assert np.all(host(y) == 0.0)
+    cfg = gen.WORKLOADS["tiny"]
+    monkeypatch.setenv("BS_FAULT", "badtable")
+    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    monkeypatch.delenv("BS_FAULT")
+    assert m.validate() == bs.BS_EBOUNDS
+    t = m.to_device(0, planned=False)
+    qLd = dev(np.zeros(cfg.NL))
+    bs.bs_scatter(t, dev(gen.uniform_pm1(1, 1, cfg.NG)), qLd)
+    assert bs.default_context().device_status() == bs.BS_EBOUNDS
+    bs.bs_gather(t, qLd, dev(np.zeros(cfg.NG)))
+    assert bs.default_context().device_status() == bs.BS_EBOUNDS
+    bs.bs_copy(x, y)
+    assert np.array_equal(host(y), np.arange(8.0))

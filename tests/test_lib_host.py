@@ -296,3 +296,18 @@ def test_plan_rejects_bad_sizes_and_oversized_smem(bs):
     assert m.plan(100, 100, 16385, 100, 2) == bs.BS_EINVAL
     assert m.plan(100, 100, 100, 100, 3) == bs.BS_EINVAL           # cluster of 3
     assert m.plan(16384, 24576, 16384, 22528, 2) == bs.BS_OK and m.plan_info().valid
+
+
+def test_fault_injection_on_the_host(bs, monkeypatch):
+    """BS_FAULT fakes failures on the host, without a GPU."""
+    monkeypatch.setenv("BS_FAULT", "alloc")
+    with pytest.raises(bs.BSError) as e:
+        bs.Context(0)
+    assert e.value.status == bs.BS_ENOMEM
+    monkeypatch.setenv("BS_FAULT", "launch,badtable")
+    assert bs.Mesh(4, 3, 1).validate() == bs.BS_EBOUNDS
+    ids = (np.arange(40, dtype=np.int32) % 7).astype(np.int32)
+    assert bs.Mesh.from_ids(ids, 7).validate() == bs.BS_EBOUNDS
+    monkeypatch.setenv("BS_FAULT", "")
+    assert bs.Mesh(4, 3, 1).validate() == bs.BS_OK
+    assert bs.Mesh.from_ids(ids, 7).validate() == bs.BS_OK
