@@ -20,7 +20,9 @@ Other modes:
                      workload (the reference arm).
   --sweep            BS1-BS5 at n = 2^10 .. 2^27, host-timed launch->sync
                      as the pages time, with the T(B) = T0 + B/Wmax fit.
-  --probe            binary64 FMA pipe throughput probe.
+  --probe            binary64 FMA pipe throughput, and the rate of scattered
+                     8-byte reads (one-pass scatter, random vs L2-resident vs
+                     sequential tables).
   --mass-operator    y = Z^T diag(d) Z x, fused against scatter + gather.
   --cg-solve         CG on Z^T diag(d) Z (GLL mass): time per iteration on
                      --config, eager launches against one CUDA-graph replay,
@@ -892,8 +894,49 @@ def run_probe(args):
         fmas = ctx.num_sms * bps * 256 * 8 * iters
         out.append({"blocks_per_sm": bps, "dfma_per_s": fmas / s, "fp64_tflops": 2 * fmas / s / 1e12,
                     "seconds": s, "sms": ctx.num_sms})
-    print(json.dumps({"mode": "probe", "dfma": out}), flush=True)
+    print(json.dumps({"mode": "probe", "dfma": out, "scattered_reads": probe_scattered(torch, bs, dev)}),
+          flush=True)
     return 0
+
+
+def probe_scattered(torch, bs, dev):
+    """Rate of scattered 8-byte reads: the one-pass scatter q_L[l] = q_G[ids[l]]
+    over the stress mesh's N_L locals with (a) random ids over a q_G beyond
+    L2, (b) random ids over a q_G that fits L2, (c) sequential ids, and the
+    two-pass scatter on table (a).  One L2 request per random read."""
+    NL = gen.WORKLOADS["stress"].NL
+    cases = {"random_ids_over_265MB": (gen.WORKLOADS["stress"].NG, True),
+             "random_ids_over_8MB_in_L2": (1 << 20, True),
+             "sequential_ids": (NL, False)}
+    res = {}
+    for name, (NG, rnd) in cases.items():
+        ids = (gen.random_scatter_ids(NG, 5, NL, NG) if rnd
+               else np.arange(NL, dtype=np.int32))
+        mesh = bs.Mesh.from_ids(ids, NG)
+        del ids
+        qG = torch.from_numpy(gen.uniform_pm1(1, 2, NG)).to(dev)
+        qL = torch.empty(NL, dtype=torch.float64, device=dev)
+        modes = [("one_pass", False)] + ([("two_pass", True)] if name.startswith("random_ids_over_265")
+                                         else [])
+        for mode, planned in modes:
+            t = mesh.to_device(0, planned=planned)
+            for _ in range(3):
+                bs.bs_scatter(t, qG, qL)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(10):
+                bs.bs_scatter(t, qG, qL)
+            e1.record()
+            e1.synchronize()
+            sec = e0.elapsed_time(e1) * 1e-3 / 10
+            res[f"{name}/{mode}"] = {"N_L": NL, "N_G": NG, "us": sec * 1e6,
+                                     "reads_per_s": NL / sec,
+                                     "GB/s_of_12NL+8NG": (12 * NL + 8 * NG) / sec / 1e9}
+            del t
+        del mesh, qG, qL
+        torch.cuda.empty_cache()
+    return res
 
 
 def traffic_from_csv(path, config):

@@ -3,9 +3,9 @@
 // Same results as the one-pass kernels of bs_gs.cu ("Portable high-order
 // finite element kernels I: Streaming Operations", BS6/BS7; eq. (3)), bit
 // for bit, with a different data movement.  On GB300 a scattered 8-byte
-// access costs one SM-to-L2 request whether it hits L2 or not, and the
-// memory system serves about 5e10 such requests per second -- a random
-// gather or scatter of N_L values cannot beat N_L / 5e10 seconds.  The plan
+// access into a vector larger than L2 pulls a whole sector from HBM, which
+// serves about 5e10 of them per second -- a random gather or scatter of N_L
+// values over such vectors cannot beat N_L / 5e10 seconds.  The plan
 // (bs_plan.cpp) instead routes every value through shared memory twice:
 //
 //   scatter pass 1 (per tile of global rows): stage the tile's q_G values in
@@ -21,9 +21,9 @@
 //     coalesced.
 //
 // Global traffic is about twice the algorithmic bytes, all of it in runs.
-// The same request rate bounds these passes: pass 1 writes runs of ~10-18
-// values, so a warp's 32 stores cost ~5 line requests instead of 2, and
-// runs grow only with tile x bucket, which one SM's shared memory caps.
+// Pass 1 writes runs of ~10-18 values, so a warp's 32 stores cost ~5 line
+// requests instead of 2; these fragmented writes set its time, and runs grow
+// only with tile x bucket, which one SM's shared memory caps.
 // One 1024-thread block per SM, up to 227 KB of dynamic shared memory.
 // Every table-derived index is checked; a bad one is skipped and raises the
 // context's device error flag.
