@@ -249,9 +249,9 @@ class Workload:
             "scatter": pm.bytes_scatter(NL, NG),
             "cg_iteration": pm.bytes_cg_iteration(NL, NG, t.nnz, t.nblocks),
         }
-        gs = 2 if self.planned else 1
-        self.launches = {"copy": 1, "axpy": 1, "norm": 1, "dot": 1, "cg_update": 1, "gather": gs,
-                         "scatter": gs, "cg_iteration": 3 + 2 * gs}
+        g_l, s_l = bs.gs_launches(cfg.NL, cfg.NG, self.planned)
+        self.launches = {"copy": 1, "axpy": 1, "norm": 1, "dot": 1, "cg_update": 1, "gather": g_l,
+                         "scatter": s_l, "cg_iteration": 3 + g_l + s_l}
         self.names = list(self.bytes)
 
     @property

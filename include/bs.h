@@ -57,6 +57,13 @@ extern "C" {
 #define BS_EALIGN (-5)  /* reserved; never returned (misalignment is peeled)       */
 #define BS_ETIMEOUT (-6) /* a bounded device-side wait gave up (see bs_ctx_device_status) */
 
+/* With a plan, bs_scatter reading a q_G of at most BS_ONEPASS_SCATTER_BYTES
+ * and bs_gather reading a q_L of at most BS_ONEPASS_GATHER_BYTES run the
+ * one-pass kernels (one launch instead of two): faster where the randomly
+ * read vector stays in L2. */
+#define BS_ONEPASS_SCATTER_BYTES (32ll << 20)
+#define BS_ONEPASS_GATHER_BYTES (8ll << 20)
+
 /* Host-side fault injection, to test a caller's error handling without
  * faulting a GPU: the environment variable BS_FAULT holds a comma-separated
  * list of "alloc" (bs_ctx_create reports BS_ENOMEM), "launch" (every call
@@ -310,7 +317,11 @@ int bs_mesh_plan_tables(const bs_mesh *mesh, const int32_t **s_tileRows,
  * skipped and raise the device error flag (see bs_ctx_device_status). */
 
 /* BS6 gather: qG[g] = (+0.0 + qL[l1]) + qL[l2] + ..., l1 < l2 < ... the
- * local copies of global node g; a row with no entries gives +0.0. */
+ * local copies of global node g; a row with no entries gives +0.0.
+ * With t->plan the two-pass kernels run, except that a q_L of at most 8 MB
+ * (BS7: a q_G of at most 32 MB) takes the one-pass kernels, faster for
+ * vectors that stay in L2 (same results; BS_TUNE_ONEPASS=0 in the
+ * environment at context creation turns this off). */
 int bs_gather(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, double *qG, void *stream);
 
 /* BS7 scatter: qL[l] = qG[scatterIds[l]], or +0.0 where scatterIds[l] < 0. */

@@ -38,6 +38,18 @@ MASK_BOUNDARY = 4
 ROTATE_ELEMS = 8
 GATHER_SEG_MAX = 4096
 GATHER_SEG_DEFAULT = 2048
+ONEPASS_SCATTER_BYTES = 32 << 20   # include/bs.h: BS_ONEPASS_SCATTER_BYTES
+ONEPASS_GATHER_BYTES = 8 << 20     # include/bs.h: BS_ONEPASS_GATHER_BYTES
+
+
+def gs_launches(NL, NG, planned):
+    """(gather, scatter) kernel launches of one bs_gather / bs_scatter call
+    with a context created under the current environment."""
+    if not planned:
+        return 1, 1
+    small = os.environ.get("BS_TUNE_ONEPASS", "1") != "0"
+    return (1 if small and 8 * NL <= ONEPASS_GATHER_BYTES else 2,
+            1 if small and 8 * NG <= ONEPASS_SCATTER_BYTES else 2)
 
 # Every symbol include/bs.h declares.
 EXPORTS = (

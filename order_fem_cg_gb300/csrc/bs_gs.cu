@@ -274,7 +274,7 @@ extern "C" int bs_gather(bs_ctx *ctx, const bs_gs_dev *t, const double *qL, doub
     if (t->NG == 0)
         return BS_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (t->plan)
+    if (t->plan && !(ctx->tune.small_onepass && 8 * t->NL <= kOnePassGatherBytes))
         return bs_gather_planned(ctx, t, qL, qG, s);
     if (t->seg_max <= 1024)
         launch_gather<1024>(ctx, t, qL, qG, s);
@@ -304,7 +304,7 @@ extern "C" int bs_scatter(bs_ctx *ctx, const bs_gs_dev *t, const double *qG, dou
     if (t->NL == 0)
         return BS_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (t->plan)
+    if (t->plan && !(ctx->tune.small_onepass && 8 * t->NG <= kOnePassScatterBytes))
         return bs_scatter_planned(ctx, t, qG, qL, s);
     const bool vec = (reinterpret_cast<uintptr_t>(t->scatterIds) & 15u) == 0 &&
                      (reinterpret_cast<uintptr_t>(qL) & 31u) == 0;

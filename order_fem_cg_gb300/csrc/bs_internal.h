@@ -22,7 +22,18 @@ struct bs_tune {
     int vec_width;             // widest vector in doubles: 4 (32 B), 2 (16 B) or 1
     int l2_prefetch;           // two-pass kernels: 0 none (default: measured fastest),
                                // 1 own inputs, 2 also the inputs of the block one wave ahead
+    int small_onepass;         // 1: one-pass gather/scatter for L2-sized vectors even with a
+                               // plan (bs_gather / bs_scatter); 0: always the plan
 };
+
+// Below these sizes of the randomly read vector the one-pass kernels beat
+// the two-pass plan on GB300 (random reads that stay in L2 run ~3.7x faster
+// than from HBM, and a two-pass call pays two launches and its phases):
+// scatter reads q_G, gather reads q_L.  Measured: scatter 23 against 42 us
+// at q_G = 22 MB, gather 9 against 29 us at q_L = 0.3 MB but 61 against
+// 56 us at q_L = 33 MB.
+constexpr int64_t kOnePassScatterBytes = BS_ONEPASS_SCATTER_BYTES;
+constexpr int64_t kOnePassGatherBytes = BS_ONEPASS_GATHER_BYTES;
 
 struct bs_ctx {
     int device;

@@ -9,6 +9,11 @@ if ROOT not in sys.path:
 
 GOLDEN = os.path.join(ROOT, "tests", "golden")
 
+# Planned gather/scatter on small meshes must exercise the two-pass kernels:
+# contexts created during the tests keep the plan whatever the size (a test
+# that wants the library default makes its own context).
+os.environ.setdefault("BS_TUNE_ONEPASS", "0")
+
 
 def build_lib():
     """Build libbs.so (if stale) without importing the package first."""

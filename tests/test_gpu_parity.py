@@ -496,3 +496,20 @@ def test_injected_faults_are_reported(monkeypatch):
     assert bs.default_context().device_status() == bs.BS_EBOUNDS
     bs.bs_copy(x, y)
     assert np.array_equal(host(y), np.arange(8.0))
+
+
+def test_small_planned_meshes_may_take_the_one_pass_kernels(monkeypatch):
+    """With the library default, a plan on an L2-sized mesh runs the one-pass
+    kernels; the results are the same bits either way."""
+    monkeypatch.setenv("BS_TUNE_ONEPASS", "1")
+    ctx = bs.Context(0)
+    for cfg in (gen.WORKLOADS["tiny"], gen.WORKLOADS["mid"]):
+        m, t, ids = mesh_case(cfg, planned=True)
+        qG = gen.uniform_pm1(cfg.seed, gen.TAG_U, cfg.NG)
+        qL = gen.uniform_pm1(cfg.seed, gen.TAG_P, cfg.NL)
+        qLd, qGd = dev(np.zeros(cfg.NL)), dev(np.zeros(cfg.NG))
+        bs.bs_scatter(t, dev(qG), qLd, ctx=ctx)
+        assert bits_equal(host(qLd), oracle.scatter(ids, qG))
+        bs.bs_gather(t, dev(qL), qGd, ctx=ctx)
+        assert bits_equal(host(qGd), oracle.gather(ids, qL, cfg.NG))
+        assert ctx.device_status() == bs.BS_OK
