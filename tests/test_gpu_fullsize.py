@@ -71,3 +71,45 @@ def test_stress_step_matches_oracle(name, planned):
     assert np.all(np.abs(rg - ref["r"]) <= da * np.abs(ref["ApG"]) + np.spacing(np.abs(ref["r"])))
     assert close(s("rnorm"), oracle.norm(rg))
     assert bs.default_context().device_status() == bs.BS_OK
+
+
+def test_stress_mass_operator_and_cg_solve():
+    """The fused global operator Z^T diag(d) Z (GLL mass) on the stress mesh,
+    bit-exact against the oracle, and three CG iterations of both solves
+    within the oracle's envelope under 1e-13 perturbations of its scalars
+    (see test_gpu_cg.py for the bound)."""
+    from test_gpu_cg import envelope
+
+    cfg = gen.WORKLOADS["stress"]
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
+    t = m.to_device(0)
+    ids = oracle_ids(cfg)
+    NG = cfg.NG
+    dL = gen.mass_diagonal(cfg.E, cfg.N)
+    x = gen.uniform_pm1(cfg.seed, gen.TAG_X, NG)
+    dLd = torch.from_numpy(dL).to(dev)
+    y = torch.empty(NG, dtype=torch.float64, device=dev)
+    bs.bs_apply_diag(t, torch.from_numpy(x).to(dev), dLd, y)
+    assert same(y.cpu().numpy(), oracle.apply_diag(ids, dL, x))
+    del y
+    b = gen.uniform_pm1(cfg.seed, gen.TAG_R, NG)
+    iters = 3
+    ref = oracle.cg_solve(ids, dL, b, np.zeros(NG), iters)
+    ex, er, err, epap = envelope(ids, dL, b, np.zeros(NG), iters, ref)
+    for fused in (False, True):
+        xd, rd, pd, Apd = (torch.zeros(NG, dtype=torch.float64, device=dev) for _ in range(4))
+        bd = torch.from_numpy(b).to(dev)
+        if fused:
+            pL = torch.empty(cfg.NL, dtype=torch.float64, device=dev)
+            s = bs.bs_cg_solve_fused(t, dLd, bd, xd, rd, pd, Apd, pL, iters).cpu().numpy()
+            del pL
+        else:
+            s = bs.bs_cg_solve(t, dLd, bd, xd, rd, pd, Apd, iters).cpu().numpy()
+        xs, rs = xd.cpu().numpy(), rd.cpu().numpy()
+        assert np.all(np.abs(s[:iters + 1] - ref["rr"]) <= 2 * err + 1e-13 * np.array(ref["rr"]))
+        assert np.max(np.abs(xs - ref["x"])) <= 2 * ex + 1e-13 * np.max(np.abs(ref["x"]))
+        assert np.max(np.abs(rs - ref["r"])) <= 2 * er + 1e-13 * np.max(np.abs(b))
+        assert bs.default_context().device_status() == bs.BS_OK
+        del xd, rd, pd, Apd, bd
