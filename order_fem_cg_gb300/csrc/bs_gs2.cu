@@ -86,6 +86,30 @@ __device__ __forceinline__ uint32_t ld_u16x2(const uint16_t *p)
     return v;
 }
 
+// Four consecutive values (32-byte aligned) and four consecutive 16-bit
+// entries (8-byte aligned), read once, not kept in L1.
+struct Quad {
+    double x, y, z, w;
+};
+
+__device__ __forceinline__ Quad ld_quad(const double *p)
+{
+    Quad v;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.f64 {%0, %1, %2, %3}, [%4];"
+                 : "=d"(v.x), "=d"(v.y), "=d"(v.z), "=d"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint2 ld_u16x4(const uint16_t *p)
+{
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v2.u32 {%0, %1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void flag(int *err)
 {
     atomicOr(err, BS_DEVERR_BOUNDS);
@@ -239,8 +263,12 @@ __device__ __forceinline__ void stage(double *dst, const double *src, int n)
 // be read two entries at a time (16-byte values, 4-byte index pairs), each
 // thread has kP pairs in flight -- twice the entries of the one-at-a-time
 // loop (kP = kU) for about the same registers, which is what a latency-
-// bound placement needs; otherwise entries are read one at a time.
-template <int kP, class F>
+// bound placement needs; otherwise entries are read one at a time.  With
+// kQuad, four at a time where both allow it (32-byte values, 8-byte index
+// quads; kP/2 quads in flight): half the load instructions, which the
+// scatter pass 2 and the fused operator (queue-throttled on global loads)
+// gain from and the gather pass 2 (at its register limit) does not.
+template <int kP, bool kQuad = false, class F>
 __device__ __forceinline__ void stream_entries(const uint16_t *idx, const double *val, int32_t j0,
                                                int32_t j1, F &&put)
 {
@@ -248,8 +276,42 @@ __device__ __forceinline__ void stream_entries(const uint16_t *idx, const double
         return;
     const uintptr_t av = reinterpret_cast<uintptr_t>(val + j0);
     const uintptr_t ai = reinterpret_cast<uintptr_t>(idx + j0);
+    const bool quad = kQuad && (av & 7u) == 0 && (ai & 1u) == 0 && ((av >> 3) & 3u) == ((ai >> 1) & 3u);
     const bool paired = (av & 7u) == 0 && (ai & 1u) == 0 && ((av >> 3) & 1u) == ((ai >> 1) & 1u);
-    if (paired) {
+    if (quad) {
+        // up to three entries first, so that val + j is 32-byte aligned
+        const int32_t h = min(static_cast<int32_t>((4u - ((av >> 3) & 3u)) & 3u), j1 - j0);
+        if (static_cast<int32_t>(threadIdx.x) < h)
+            put(ld_u16(idx + j0 + threadIdx.x), ld_seq(val + j0 + threadIdx.x));
+        const int32_t j = j0 + h;
+        const int32_t nq = (j1 - j) >> 2;
+        const double *vp = val + j;
+        const uint16_t *ip = idx + j;
+        constexpr int kQ = (kP + 1) / 2;
+        for (int32_t q = threadIdx.x; q < nq; q += kQ * kT) {
+            Quad v[kQ];
+            uint2 p[kQ];
+#pragma unroll
+            for (int i = 0; i < kQ; ++i) {
+                const int32_t qq = q + i * kT;
+                v[i] = qq < nq ? ld_quad(vp + 4 * qq) : Quad{0.0, 0.0, 0.0, 0.0};
+                p[i] = qq < nq ? ld_u16x4(ip + 4 * qq) : make_uint2(0u, 0u);
+            }
+#pragma unroll
+            for (int i = 0; i < kQ; ++i)
+                if (q + i * kT < nq) {
+                    put(p[i].x & 0xffffu, v[i].x);
+                    put(p[i].x >> 16, v[i].y);
+                    put(p[i].y & 0xffffu, v[i].z);
+                    put(p[i].y >> 16, v[i].w);
+                }
+        }
+        // the last (j1 - j) mod 4 entries
+        const int32_t t0 = j + 4 * nq;
+        const int32_t lt = static_cast<int32_t>(threadIdx.x) - 32;
+        if (lt >= 0 && lt < j1 - t0)
+            put(ld_u16(idx + t0 + lt), ld_seq(val + t0 + lt));
+    } else if (paired) {
         int32_t j = j0;
         if ((av >> 3) & 1u) {  // one entry first, so that val + j is 16-byte aligned
             if (threadIdx.x == 0)
@@ -729,7 +791,7 @@ __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, doubl
         const int32_t n = j1 - j0;
         const int32_t jb = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * r / CS);
         const int32_t je = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * (r + 1) / CS);
-        stream_entries<CS == 1 ? kU : 6>(a.s_dst, a.work, jb, je, [&](uint32_t d, double v) {
+        stream_entries<CS == 1 ? kU : 6, true>(a.s_dst, a.work, jb, je, [&](uint32_t d, double v) {
             if (d < static_cast<uint32_t>(len)) {
                 const int owner = CS == 1 ? 0 : d / per;
                 pick<CS>(dst, owner)[d - owner * per] = v;
@@ -1014,7 +1076,7 @@ __global__ void __launch_bounds__(kT, 1)
     __syncthreads();  // zeroed
     bool bad = false;
     if (ok) {
-        stream_entries<6>(a.s_dst, ws, j0, j1, [&](uint32_t d, double v) {
+        stream_entries<6, true>(a.s_dst, ws, j0, j1, [&](uint32_t d, double v) {
             if (d < static_cast<uint32_t>(len))
                 vals[d] = v;
             else
