@@ -781,8 +781,11 @@ __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, doubl
     const int32_t j0 = a.s_runStart[b];
     const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + b];
     const bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len;
-    for (int32_t i = threadIdx.x; i < mine; i += kT)
-        out[i] = 0.0;
+    // pre-zeroed for masked locals; a bucket with as many entries as locals
+    // has none (every local has exactly one entry), and every slot is placed
+    if (!(ok && j1 - j0 == len))
+        for (int32_t i = threadIdx.x; i < mine; i += kT)
+            out[i] = 0.0;
     double *dst[CS];
     map_cluster<CS>(out, dst);
     cluster_barrier<CS>();  // every block's slice is zeroed
@@ -1070,8 +1073,9 @@ __global__ void __launch_bounds__(kT, 1)
     const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
     bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len && s0 >= 0 &&
               s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
-    for (int32_t i = threadIdx.x; i < len; i += kT)
-        vals[i] = 0.0;
+    if (!(ok && j1 - j0 == len))  // (no masked local: every slot is placed)
+        for (int32_t i = threadIdx.x; i < len; i += kT)
+            vals[i] = 0.0;
     const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
     __syncthreads();  // zeroed
     bool bad = false;
