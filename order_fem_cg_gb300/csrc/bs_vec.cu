@@ -9,6 +9,8 @@
 //    stride over 32-byte vectors (ld/st.global.v4.f64, sm_100+), UNROLL
 //    independent vectors per operand in flight per thread;
 //  * loads skip L1 (L1::no_allocate) and ask L2 for 256-byte prefetch;
+//    stores are streaming (.cs: evict first), so a kernel's written lines
+//    leave L2 while it runs instead of during the next kernel;
 //  * a misaligned head (< 4 elements) and the ragged tail are done by the
 //    first threads of the grid with scalar accesses;
 //  * reductions (BS3-BS5) are one launch: each block reduces its threads'
@@ -71,7 +73,7 @@ __device__ __forceinline__ void st_stream(double *p, const Vec<V> &r);
 template <>
 __device__ __forceinline__ void st_stream<4>(double *p, const Vec<4> &r)
 {
-    asm volatile("st.global.L1::no_allocate.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(p), "d"(r.v[0]),
+    asm volatile("st.global.cs.v4.f64 [%0], {%1,%2,%3,%4};" ::"l"(p), "d"(r.v[0]),
                  "d"(r.v[1]), "d"(r.v[2]), "d"(r.v[3])
                  : "memory");
 }
@@ -79,7 +81,7 @@ __device__ __forceinline__ void st_stream<4>(double *p, const Vec<4> &r)
 template <>
 __device__ __forceinline__ void st_stream<2>(double *p, const Vec<2> &r)
 {
-    asm volatile("st.global.L1::no_allocate.v2.f64 [%0], {%1,%2};" ::"l"(p), "d"(r.v[0]),
+    asm volatile("st.global.cs.v2.f64 [%0], {%1,%2};" ::"l"(p), "d"(r.v[0]),
                  "d"(r.v[1])
                  : "memory");
 }
@@ -87,7 +89,7 @@ __device__ __forceinline__ void st_stream<2>(double *p, const Vec<2> &r)
 template <>
 __device__ __forceinline__ void st_stream<1>(double *p, const Vec<1> &r)
 {
-    asm volatile("st.global.L1::no_allocate.f64 [%0], %1;" ::"l"(p), "d"(r.v[0]) : "memory");
+    asm volatile("st.global.cs.f64 [%0], %1;" ::"l"(p), "d"(r.v[0]) : "memory");
 }
 
 // Elements [0, h) and [h + nv V, h + nv V + t) are scalars; element index
