@@ -227,6 +227,36 @@ def check_scatter_gather(cfg, m, t, ids):
     assert bs.default_context().device_status() == bs.BS_OK
 
 
+@pytest.mark.parametrize("idx_off,work_off", [(0, 0), (1, 0), (2, 0), (3, 1), (0, 1), (2, 3)])
+def test_two_pass_with_shifted_plan_tables(idx_off, work_off):
+    """Pass 2 reads its work entries four, two or one at a time depending on
+    how the 16-bit position tables and the work array line up; shifting them
+    (16-bit and 8-byte steps) runs every one of those paths, on a masked mesh
+    (zeroed buckets) and its unmasked twin, for scatter, gather and the fused
+    diagonal operator."""
+    for flags in (7, 3):
+        cfg = gen.MeshConfig("shift", 6, 4, 23, flags)
+        m, t, ids = mesh_case(cfg, planned=True, sizes=(300, 500, 500, 400, 1))
+        keep = []
+        for name in ("s_dst", "g_pos"):
+            src = t.plan[name]
+            buf = torch.zeros(src.numel() + 4, dtype=torch.int16, device=DEV)
+            buf[idx_off:idx_off + src.numel()] = src
+            keep.append(buf)
+            setattr(t.plan_struct, name, buf.data_ptr() + 2 * idx_off)
+        work = torch.empty(2 * m.nnz + 4, dtype=torch.float64, device=DEV)
+        keep.append(work)
+        t.plan_struct.work = work.data_ptr() + 8 * work_off
+        check_scatter_gather(cfg, m, t, ids)
+        dL = gen.uniform_range(cfg.seed, 1, cfg.NL, 0.5, 1.5)
+        x = gen.uniform_pm1(cfg.seed, 2, cfg.NG)
+        y = torch.empty(cfg.NG, dtype=torch.float64, device=DEV)
+        bs.bs_apply_diag(t, dev(x), dev(dL), y)
+        assert bits_equal(host(y), oracle.apply_diag(ids, dL, x))
+        assert bs.default_context().device_status() == bs.BS_OK
+        del keep
+
+
 @pytest.mark.parametrize("NL,NG,masked,planned", [
     (20000, 4000, 40, False), (20000, 4000, 40, True), (300000, 120000, 0, True),
     (3000, 100, 0, False), (3000, 100, 0, True), (2000000, 400000, 25, True),
