@@ -381,14 +381,16 @@ __device__ void block_exclusive_scan(T *a, int n)
         warp_tot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        T w = warp_tot[lane];
+        constexpr int kWarps = kT / 32;  // <= 32
+        T w = lane < kWarps ? warp_tot[lane] : T(0);
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const T y = __shfl_up_sync(0xffffffffu, w, o);
             if (lane >= o)
                 w += y;
         }
-        warp_tot[lane] = w;
+        if (lane < kWarps)
+            warp_tot[lane] = w;
     }
     __syncthreads();
     T prefix = (v - local) + (warp > 0 ? warp_tot[warp - 1] : T(0));
