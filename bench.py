@@ -20,9 +20,6 @@ Other modes:
                      workload (the reference arm).
   --sweep            BS1-BS5 at n = 2^10 .. 2^27, host-timed launch->sync
                      as the pages time, with the T(B) = T0 + B/Wmax fit.
-  --probe            binary64 FMA pipe throughput, and the rate of scattered
-                     8-byte reads (one-pass scatter, random vs L2-resident vs
-                     sequential tables).
   --mass-operator    y = Z^T diag(d) Z x, fused against scatter + gather.
   --cg-solve         CG on Z^T diag(d) Z (GLL mass): time per iteration on
                      --config, eager launches against one CUDA-graph replay,
@@ -88,7 +85,6 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true")
-    ap.add_argument("--probe", action="store_true")
     ap.add_argument("--mass-operator", action="store_true",
                     help="time y = Z^T diag(d) Z x (fused, GLL mass diagonal) against a "
                          "separate scatter + gather on --config")
@@ -367,9 +363,48 @@ class Workload:
             self.ev_scalars_out.record(self.s_out)
 
 
+_PERFMODEL = None
+
+
 def bs_perf():
-    from order_fem_cg_gb300 import perfmodel
-    return perfmodel
+    """order_fem_cg_gb300/perfmodel.py (byte counts, eqs. (8)-(10)) loaded by
+    path: importing the package would map libbs.so, and the reference arm
+    runs the oracle alone."""
+    global _PERFMODEL
+    if _PERFMODEL is None:
+        import importlib.util
+        path = os.path.join(ROOT, "order_fem_cg_gb300", "perfmodel.py")
+        spec = importlib.util.spec_from_file_location("_bs_perfmodel", path)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        _PERFMODEL = mod
+    return _PERFMODEL
+
+
+def host_cpu():
+    """The host's logical CPU count and model name (the CPU legs' context)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine(),
+            "machine": platform.machine()}
 
 
 # --------------------------------------------------------- oracle (CPU) leg
@@ -453,7 +488,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(cfg, args.gpus),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": samp.describe()},
+                         "sample": samp.describe(), "host": host_cpu()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -610,7 +645,8 @@ def run_gpu(args):
             if dt >= args.cpu_seconds or reps >= 50:
                 break
         cpu = {"value": samp.bytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
-               "kind": "oracle", "sample": f"{reps} x " + samp.describe(), "seconds": dt}
+               "kind": "oracle", "sample": f"{reps} x " + samp.describe(), "seconds": dt,
+               "host": host_cpu()}
 
     if rank == 0:
         line = {
@@ -871,74 +907,6 @@ def run_cg_solve(args):
     return 0
 
 
-def run_probe(args):
-    import torch
-
-    import order_fem_cg_gb300 as bs
-
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    sink = torch.zeros(1, dtype=torch.float64, device=dev)
-    ctx = bs.default_context()
-    out = []
-    for bps in (4, 8):
-        iters = 20000
-        bs.bs_probe_dfma(bps, 100, sink)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        bs.bs_probe_dfma(bps, iters, sink)
-        e1.record()
-        e1.synchronize()
-        s = e0.elapsed_time(e1) * 1e-3
-        fmas = ctx.num_sms * bps * 256 * 8 * iters
-        out.append({"blocks_per_sm": bps, "dfma_per_s": fmas / s, "fp64_tflops": 2 * fmas / s / 1e12,
-                    "seconds": s, "sms": ctx.num_sms})
-    print(json.dumps({"mode": "probe", "dfma": out, "scattered_reads": probe_scattered(torch, bs, dev)}),
-          flush=True)
-    return 0
-
-
-def probe_scattered(torch, bs, dev):
-    """Rate of scattered 8-byte reads: the one-pass scatter q_L[l] = q_G[ids[l]]
-    over the stress mesh's N_L locals with (a) random ids over a q_G beyond
-    L2, (b) random ids over a q_G that fits L2, (c) sequential ids, and the
-    two-pass scatter on table (a).  One L2 request per random read."""
-    NL = gen.WORKLOADS["stress"].NL
-    cases = {"random_ids_over_265MB": (gen.WORKLOADS["stress"].NG, True),
-             "random_ids_over_8MB_in_L2": (1 << 20, True),
-             "sequential_ids": (NL, False)}
-    res = {}
-    for name, (NG, rnd) in cases.items():
-        ids = (gen.random_scatter_ids(NG, 5, NL, NG) if rnd
-               else np.arange(NL, dtype=np.int32))
-        mesh = bs.Mesh.from_ids(ids, NG)
-        del ids
-        qG = torch.from_numpy(gen.uniform_pm1(1, 2, NG)).to(dev)
-        qL = torch.empty(NL, dtype=torch.float64, device=dev)
-        modes = [("one_pass", False)] + ([("two_pass", True)] if name.startswith("random_ids_over_265")
-                                         else [])
-        for mode, planned in modes:
-            t = mesh.to_device(0, planned=planned)
-            for _ in range(3):
-                bs.bs_scatter(t, qG, qL)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(10):
-                bs.bs_scatter(t, qG, qL)
-            e1.record()
-            e1.synchronize()
-            sec = e0.elapsed_time(e1) * 1e-3 / 10
-            res[f"{name}/{mode}"] = {"N_L": NL, "N_G": NG, "us": sec * 1e6,
-                                     "reads_per_s": NL / sec,
-                                     "GB/s_of_12NL+8NG": (12 * NL + 8 * NG) / sec / 1e9}
-            del t
-        del mesh, qG, qL
-        torch.cuda.empty_cache()
-    return res
-
-
 def traffic_from_csv(path, config):
     """Per-operation DRAM bytes per call from an ncu launch list of bench steps."""
     import csv
@@ -985,8 +953,6 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
-    if args.probe:
-        return run_probe(args)
     if args.mass_operator:
         return run_mass_operator(args)
     if args.cg_solve:

@@ -405,36 +405,37 @@ int bs_cg_solve_fused(bs_ctx *ctx, const bs_gs_dev *t, const double *dL, const d
  * bs_ctx_device_status reports BS_ETIMEOUT.  Nothing faults or hangs. */
 int bs_probe_grid_barrier(bs_ctx *ctx, int absent_block, void *stream);
 
-/* ---- diagnostics ----------------------------------------------------------
- * Throughput probe of the binary64 fused multiply-add pipe: launches
- * `blocks_per_sm` x SMs blocks of 256 threads, each thread running `iters`
- * rounds of 8 independent fma chains (16 flops per round and chain pair),
- * and writes a checksum to *sink_dev.  Time it with events on `stream`:
- * DFMA/s = SMs * blocks_per_sm * 256 * 8 * iters / seconds. */
-int bs_probe_dfma(bs_ctx *ctx, int blocks_per_sm, int64_t iters, double *sink_dev, void *stream);
-
 /* ---- allocation-free inner product ----------------------------------------
  * The paper has no counterpart to this entry point; it is a library
  * convenience.  For callers that cannot call cudaMalloc -- code running
- * inside a device-memory allocator's hooks or a host callback, or an
- * embedding runtime that owns every device allocation -- and therefore
- * cannot create a bs_ctx (a context allocates its reduction workspace).
+ * inside a device-memory allocator's own hooks, where an allocation would
+ * recurse into the allocator, or an embedding runtime that owns every
+ * device allocation -- and therefore cannot create a bs_ctx (a context
+ * allocates its reduction workspace).
  *
  * Computes *out_dev = sum_i x[i] y[i] like bs_dot, with the same kernel,
  * but keeps the per-block partial sums and the completion counter in one
  * static device array of 8,448 bytes (1,024 partial sums plus the
  * counter) that every GPU loading this library holds until the process
  * exits.  It calls no cudaMalloc, cudaFree or allocating library routine.
- *  - Uses the calling thread's current device.  The first call on a device
- *    looks up the array's device address (cudaGetSymbolAddress) and the SM
- *    count; make that first call before any stream capture.
+ *  - Uses the calling thread's current device; x, y and out_dev must be
+ *    memory of that device.  Every call looks up the array's device address
+ *    (cudaGetSymbolAddress) and the SM count, so it stays valid across
+ *    cudaDeviceReset.  The first call in a process may load the library's
+ *    device code (lazy module loading); make it before any stream capture.
+ *  - Do not call it from inside a CUDA host function or stream callback:
+ *    CUDA forbids CUDA API calls there, and this call issues a memset and a
+ *    kernel launch.
  *  - Each call first clears the counter on `stream` (the array keeps the
  *    previous call's contents).  All calls share the one array, so calls
  *    whose work overlaps on the GPU (other streams, other threads) race and
  *    give wrong results: serialise them.
  *  - BS_EINVAL if the device would need more than 1,024 partial sums
  *    (more than 256 SMs) or on a bad argument; BS_ECUDA on a CUDA error.
- *    There is no context, so there is no error message beyond the code. */
+ *    If a CUDA error is already pending on the calling thread (left by
+ *    earlier work), the call returns BS_ECUDA, launches nothing and leaves
+ *    that error pending for its owner.  There is no context, so there is
+ *    no error message beyond the code. */
 int bs_dot_noalloc(int64_t n, const double *x, const double *y, double *out_dev, void *stream);
 
 #ifdef __cplusplus

@@ -57,7 +57,7 @@ EXPORTS = (
     "bs_ctx_device_status", "bs_copy", "bs_axpy", "bs_norm", "bs_dot", "bs_cg_update",
     "bs_mesh_build_box", "bs_mesh_build_box_ex", "bs_mesh_info", "bs_mesh_tables",
     "bs_mesh_validate", "bs_mesh_destroy", "bs_gather", "bs_scatter", "bs_cg_iteration",
-    "bs_probe_dfma", "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
+    "bs_dot_noalloc", "bs_mesh_plan", "bs_mesh_plan_info", "bs_mesh_plan_tables",
     "bs_apply_diag", "bs_axpy_dev", "bs_cg_solve", "bs_cg_solve_fused", "bs_probe_grid_barrier",
     "bs_mesh_from_ids",
 )
@@ -142,7 +142,6 @@ def _declare(lib):
                               [ctypes.c_int32, _vp, _vp], _int),
         "bs_probe_grid_barrier": ([_vp, _int, _vp], _int),
         "bs_mesh_from_ids": ([_i64, _i64, _vp, ctypes.c_int32, ctypes.POINTER(_vp)], _int),
-        "bs_probe_dfma": ([_vp, _int, _i64, _vp, _vp], _int),
         "bs_dot_noalloc": ([_i64, _vp, _vp, _vp, _vp], _int),
         "bs_mesh_plan": ([_vp] + [ctypes.c_int32] * 5, _int),
         "bs_mesh_plan_info": ([_vp, ctypes.POINTER(PlanInfo)], _int),
@@ -324,19 +323,18 @@ def bs_dot_noalloc(x, y, out, stream=None):
 
     Same result as bs_dot, with the reduction's scratch in a static device
     array shared by all calls (serialise calls; `out` must be preallocated).
+    x, y and out must live on the current CUDA device: the call launches
+    there and has no context to check against.
     """
+    cur = torch.cuda.current_device()
+    for name, t in (("x", x), ("y", y), ("out", out)):
+        if isinstance(t, torch.Tensor) and t.is_cuda and t.device.index != cur:
+            raise ValueError(f"{name} is on {t.device}, not on the current device cuda:{cur}")
     st = lib.bs_dot_noalloc(x.numel(), _vec(x, "x"), _vec(y, "y", x.numel()), _vec(out, "out", 1),
                             _stream(stream))
     if st != BS_OK:
         raise BSError(st, "bs_dot_noalloc")
     return out
-
-
-def bs_probe_dfma(blocks_per_sm, iters, sink, stream=None, ctx=None):
-    """Launch the binary64 FMA throughput probe (diagnostic)."""
-    ctx = _ctx(ctx, sink)
-    ctx.check(lib.bs_probe_dfma(ctx.handle, int(blocks_per_sm), int(iters), _vec(sink, "sink"),
-                                _stream(stream)), "bs_probe_dfma")
 
 
 # ------------------------------------------------------------- mesh

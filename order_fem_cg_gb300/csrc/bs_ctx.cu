@@ -109,7 +109,8 @@ extern "C" int bs_ctx_create(int device, bs_ctx **out)
         ctx->tune.reduce_blocks_per_sm = env_int("BS_TUNE_REDUCE_BPS", 4, 1, 32);
         ctx->tune.scatter_blocks_per_sm = env_int("BS_TUNE_SCATTER_BPS", 8, 1, 32);
         ctx->tune.vec_width = env_int("BS_TUNE_VEC", 4, 1, 4);
-        ctx->tune.l2_prefetch = env_int("BS_TUNE_L2PF", 0, 0, 2);
+        ctx->tune.persist = env_int("BS_TUNE_PERSIST", 0, 0, 1);
+        ctx->tune.l2_prefetch = env_int("BS_TUNE_L2PF", 1, 0, 1);
         ctx->tune.small_onepass = env_int("BS_TUNE_ONEPASS", 1, 0, 1);
         if (ctx->tune.vec_width == 3)
             ctx->tune.vec_width = 2;

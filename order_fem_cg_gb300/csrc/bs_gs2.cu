@@ -51,7 +51,7 @@ struct PlanArgs {
     const uint16_t *g_src, *g_pos, *g_groupStart, *g_rowPos;
     double *work;
     int *err;
-    int pf_mode, pf_ahead;  // L2 prefetch of sequential inputs (see prefetch_l2)
+    int pf_next;  // persistent grids: prefetch a block's next tile/bucket into L2
 };
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p)
@@ -141,18 +141,19 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
-// Waits for phase 0 of the barrier; gives up after a bounded number of
-// polls (each poll may suspend the thread briefly) and reports false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar)
+// Waits for the completion of the barrier's phase of the given parity
+// (0 for its first use, then alternating); gives up after a bounded number
+// of polls (each poll may suspend the thread briefly) and reports false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     constexpr uint32_t kMaxPolls = 1u << 24;
     for (uint32_t i = 0; i < kMaxPolls; ++i) {
         uint32_t done;
         asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                      "selp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(done)
-                     : "r"(smem_u32(bar))
+                     : "r"(smem_u32(bar)), "r"(parity)
                      : "memory");
         if (done)
             return true;
@@ -160,35 +161,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar)
     return false;
 }
 
-// Waits for a bulk staging started by stage_start: thread 0 polls the
-// barrier (bounded) while the other threads wait at the block barrier, so
-// the wait issues almost no instructions; a wait that ran out is followed
-// by one more bounded wait for the copy still in flight.  Afterwards every
-// thread tests the (completed) phase once, which is its own acquire of the
-// copied data.  Returns the outcome in every thread.
-__device__ __forceinline__ bool stage_wait(bool bulk, uint64_t *bar)
+// Waits for a bulk staging started by stage_start (barrier phase of the
+// given parity): thread 0 polls the barrier (bounded) while the other
+// threads wait at the block barrier, so the wait issues almost no
+// instructions; a wait that ran out is followed by one more bounded wait
+// for the copy still in flight.  Afterwards every thread tests the
+// (completed) phase once, which is its own acquire of the copied data.
+// Returns the outcome in every thread; after a failed wait the caller
+// stops using the barrier (its phase is no longer known).
+__device__ __forceinline__ bool stage_wait(bool bulk, uint64_t *bar, uint32_t parity)
 {
     __shared__ int s_staged;
     if (threadIdx.x == 0) {
         int ok = 1;
-        if (bulk && !mbar_wait(bar)) {
+        if (bulk && !mbar_wait(bar, parity)) {
             ok = 0;
-            mbar_wait(bar);
+            mbar_wait(bar, parity);
         }
         s_staged = ok;
     }
     __syncthreads();
-    if (bulk && s_staged) {
+    const bool staged = s_staged != 0;
+    if (bulk && staged) {
         uint32_t done;
         asm volatile("{\n\t.reg .pred p;\n\t"
-                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                      "selp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(done)
-                     : "r"(smem_u32(bar))
+                     : "r"(smem_u32(bar)), "r"(parity)
                      : "memory");
         (void)done;
     }
-    return s_staged != 0;
+    __syncthreads();  // s_staged is rewritten by the next wait
+    return staged;
 }
 
 // Asks the bulk-copy engine to bring [p, p + bytes) into L2 (no data to the
@@ -227,12 +232,13 @@ __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t 
 }
 
 // Stages n consecutive doubles into shared memory: by the bulk-copy engine
-// when the source is 16-byte aligned (an odd last element by a thread),
-// else by the threads.  `bar` must be initialised; every thread calls it
-// and later calls stage_wait with the returned flag.
-__device__ __forceinline__ bool stage_start(double *dst, const double *src, int n, uint64_t *bar)
+// when the source is 16-byte aligned and `use_bulk` (an odd last element
+// by a thread), else by the threads.  `bar` must be initialised; every
+// thread calls it and later calls stage_wait with the returned flag.
+__device__ __forceinline__ bool stage_start(double *dst, const double *src, int n, uint64_t *bar,
+                                            bool use_bulk = true)
 {
-    const bool bulk = n >= 2 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
+    const bool bulk = use_bulk && n >= 2 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0;
     if (bulk) {
         if (threadIdx.x == 0)
             bulk_load(dst, src, static_cast<uint32_t>(n & ~1) * 8u, bar);
@@ -651,11 +657,15 @@ __device__ __forceinline__ void map_cluster(double *mine, double **all)
     }
 }
 
-// ------------------------------------------- L2 prefetch of a block's inputs
-// Thread 0 of a block asks for its own block's sequential inputs and, with
-// pf_mode 2, for those of the block one wave (pf_ahead blocks) later, which
-// will run on some SM soon: L2 then stages what shared memory has no room
-// for.  Ranges come from the tables, clamped into the arrays.
+// ------------------------------------------- L2 prefetch of a block's next item
+// In a persistent grid each block takes items blockIdx, blockIdx + step, ...
+// (step = the number of blocks or clusters), so it knows its next tile or
+// bucket; one lane asks the bulk-copy engine to bring that item's
+// sequential inputs into L2 while the block works on the current one, so
+// that the next staging or placement reads L2 instead of waiting on HBM.
+// Ranges come from the tables, clamped into the arrays.
+__device__ __forceinline__ bool pf_lane() { return threadIdx.x == kT - 32; }
+
 __device__ void pf_scatter_tile(const PlanArgs &a, int t, const double *qG)
 {
     const int64_t B = a.s_nbuckets;
@@ -704,9 +714,27 @@ __device__ void pf_gather_bucket(const PlanArgs &a, int c, const double *wg)
     }
 }
 
+// Block-uniform "a bulk staging wait ran out": the barrier's phase is then
+// unknown, so the block stops using bulk copies for the rest of the launch.
+struct StageState {
+    uint32_t parity = 0;
+    bool broken = false;
+};
+
+__device__ __forceinline__ bool stage_done(StageState &st, bool bulk, uint64_t *bar)
+{
+    const bool staged = stage_wait(bulk, bar, st.parity);
+    if (bulk)
+        st.parity ^= 1u;
+    if (!staged)
+        st.broken = true;
+    return staged;
+}
+
 // --------------------------------------------------------------- scatter
 // One cluster per tile of CS * s_tile_rows global rows; block r stages rows
 // [r * s_tile_rows, (r+1) * s_tile_rows) of it and emits 1/CS of the slots.
+// A grid with fewer clusters than tiles loops over tiles (persistent).
 template <int CS>
 __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const double *__restrict__ qG)
 {
@@ -714,116 +742,123 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
     double *vals = reinterpret_cast<double *>(smem);
     int64_t *runs = reinterpret_cast<int64_t *>(vals + a.s_tile_rows);
     int32_t *runD = reinterpret_cast<int32_t *>(runs + a.s_nbuckets + 1);
-    const int r = cluster_rank<CS>();
-    const int t = blockIdx.x / CS;
-    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
-        pf_scatter_tile(a, t, qG);
-        if (a.pf_mode > 1 && t + a.pf_ahead < a.s_ntiles)
-            pf_scatter_tile(a, t + a.pf_ahead, qG);
-    }
-    // The plan's tiles are the row ranges [t TR, (t+1) TR) clipped to N_G,
-    // so the staging starts without waiting for a table; s_tileRows and
-    // the CSR entry range are loaded meanwhile and checked before use.
-    const int64_t TR = static_cast<int64_t>(CS) * a.s_tile_rows;
-    const int32_t r0 = static_cast<int32_t>(min(t * TR, a.NG));
-    const int32_t r1 = static_cast<int32_t>(min((t + 1) * TR, a.NG));
-    const int32_t nrows = r1 - r0;
-    const int32_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
-    bool ok = a.s_tileRows[t] == r0 && a.s_tileRows[t + 1] == r1;
     __shared__ uint64_t bar;
     if (threadIdx.x == 0)
         mbar_init(&bar);
     __syncthreads();
-    const int32_t m0 = min(r * a.s_tile_rows, nrows);
-    const int32_t m1 = min((r + 1) * a.s_tile_rows, nrows);
-    const bool bulk = stage_start(vals, qG + r0 + m0, m1 - m0, &bar);
-    ok = ok && e0 >= 0 && e1 >= e0 && e1 <= a.nnz;
-    const RunFetch rf = fetch_runs(a.s_runStart, t, a.s_nbuckets);
-    if (!bulk)
-        stage(vals, qG + r0 + m0, m1 - m0);
-    ok = commit_runs(rf, a.s_runStart, t, a.s_nbuckets, a.nnz, runs, runD) && ok &&
-         run_off(runs[a.s_nbuckets]) == e1 - e0;
-    ok = stage_wait(bulk, &bar) && ok;
+    const int r = cluster_rank<CS>();
+    const int step = static_cast<int>(gridDim.x) / CS;
     double *tile[CS];
     map_cluster<CS>(vals, tile);
-    cluster_barrier<CS>();  // every block's slice is staged
-    if (ok) {
-        const int32_t total = e1 - e0;
-        const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
-        const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
-        if (emit_runs<CS>(runs, runD, a.s_nbuckets, kb, ke, a.s_src, e0, tile, a.s_tile_rows,
-                          nrows, a.work, a.nnz))
+    StageState st;
+    for (int t = static_cast<int>(blockIdx.x) / CS; t < a.s_ntiles; t += step) {
+        // The plan's tiles are the row ranges [t TR, (t+1) TR) clipped to
+        // N_G, so the staging starts without waiting for a table;
+        // s_tileRows and the CSR entry range are loaded meanwhile and
+        // checked before use.
+        const int64_t TR = static_cast<int64_t>(CS) * a.s_tile_rows;
+        const int32_t r0 = static_cast<int32_t>(min(t * TR, a.NG));
+        const int32_t r1 = static_cast<int32_t>(min((t + 1) * TR, a.NG));
+        const int32_t nrows = r1 - r0;
+        const int32_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
+        bool ok = a.s_tileRows[t] == r0 && a.s_tileRows[t + 1] == r1 && !st.broken;
+        const int32_t m0 = min(r * a.s_tile_rows, nrows);
+        const int32_t m1 = min((r + 1) * a.s_tile_rows, nrows);
+        const bool bulk = stage_start(vals, qG + r0 + m0, m1 - m0, &bar, !st.broken);
+        ok = ok && e0 >= 0 && e1 >= e0 && e1 <= a.nnz;
+        const RunFetch rf = fetch_runs(a.s_runStart, t, a.s_nbuckets);
+        if (!bulk)
+            stage(vals, qG + r0 + m0, m1 - m0);
+        ok = commit_runs(rf, a.s_runStart, t, a.s_nbuckets, a.nnz, runs, runD) && ok &&
+             run_off(runs[a.s_nbuckets]) == e1 - e0;
+        ok = stage_done(st, bulk, &bar) && ok;
+        if (a.pf_next && pf_lane() && t + step < a.s_ntiles)
+            pf_scatter_tile(a, t + step, qG);
+        cluster_barrier<CS>();  // every block's slice is staged
+        if (ok) {
+            const int32_t total = e1 - e0;
+            const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
+            const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
+            if (emit_runs<CS>(runs, runD, a.s_nbuckets, kb, ke, a.s_src, e0, tile, a.s_tile_rows,
+                              nrows, a.work, a.nnz))
+                flag(a.err);
+        } else if (threadIdx.x == 0) {
             flag(a.err);
-    } else if (threadIdx.x == 0) {
-        flag(a.err);
+        }
+        cluster_barrier<CS>();  // peers may still read this block's slice
     }
-    cluster_barrier<CS>();  // peers may still read this block's slice
 }
 
 // One cluster per bucket of CS * s_bucket_len locals; block r holds locals
 // [r * s_bucket_len, (r+1) * s_bucket_len) of it and places 1/CS of the
-// bucket's work entries (into any block of the cluster).
+// bucket's work entries (into any block of the cluster).  A grid with
+// fewer clusters than buckets loops over buckets (persistent).
 template <int CS>
 __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, double *__restrict__ qL)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     double *out = reinterpret_cast<double *>(smem);
     const int r = cluster_rank<CS>();
-    const int b = blockIdx.x / CS;
-    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
-        pf_scatter_bucket(a, b, a.work);
-        if (a.pf_mode > 1 && b + a.pf_ahead < a.s_nbuckets)
-            pf_scatter_bucket(a, b + a.pf_ahead, a.work);
-    }
-    const int32_t per = a.s_bucket_len;
-    const int64_t l0 = static_cast<int64_t>(b) * CS * per;
-    const int64_t rest = a.NL - l0;
-    const int32_t len = static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
-    const int32_t mine = max(0, min(per, len - r * per));
-    const int32_t j0 = a.s_runStart[b];
-    const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + b];
-    const bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len;
-    // pre-zeroed for masked locals; a bucket with as many entries as locals
-    // has none (every local has exactly one entry), and every slot is placed
-    if (!(ok && j1 - j0 == len))
-        for (int32_t i = threadIdx.x; i < mine; i += kT)
-            out[i] = 0.0;
+    const int step = static_cast<int>(gridDim.x) / CS;
     double *dst[CS];
     map_cluster<CS>(out, dst);
-    cluster_barrier<CS>();  // every block's slice is zeroed
-    bool bad = !ok;
-    if (ok) {
-        const int32_t n = j1 - j0;
-        const int32_t jb = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * r / CS);
-        const int32_t je = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * (r + 1) / CS);
-        stream_entries<CS == 1 ? kU : 6, true>(a.s_dst, a.work, jb, je, [&](uint32_t d, double v) {
-            if (d < static_cast<uint32_t>(len)) {
-                const int owner = CS == 1 ? 0 : d / per;
-                pick<CS>(dst, owner)[d - owner * per] = v;
-            } else {
-                bad = true;
-            }
-        });
+    for (int b = static_cast<int>(blockIdx.x) / CS; b < a.s_nbuckets; b += step) {
+        if (a.pf_next && pf_lane() && b + step < a.s_nbuckets)
+            pf_scatter_bucket(a, b + step, a.work);
+        const int32_t per = a.s_bucket_len;
+        const int64_t l0 = static_cast<int64_t>(b) * CS * per;
+        const int64_t rest = a.NL - l0;
+        const int32_t len =
+            static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
+        const int32_t mine = max(0, min(per, len - r * per));
+        const int32_t j0 = a.s_runStart[b];
+        const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + b];
+        const bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len;
+        // pre-zeroed for masked locals; a bucket with as many entries as
+        // locals has none (every local has exactly one entry), and every
+        // slot is placed
+        if (!(ok && j1 - j0 == len))
+            for (int32_t i = threadIdx.x; i < mine; i += kT)
+                out[i] = 0.0;
+        cluster_barrier<CS>();  // every block's slice is zeroed
+        bool bad = !ok;
+        if (ok) {
+            const int32_t n = j1 - j0;
+            const int32_t jb = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * r / CS);
+            const int32_t je = j0 + static_cast<int32_t>(static_cast<int64_t>(n) * (r + 1) / CS);
+            stream_entries<CS == 1 ? kU : 6, true>(a.s_dst, a.work, jb, je, [&](uint32_t d, double v) {
+                if (d < static_cast<uint32_t>(len)) {
+                    const int owner = CS == 1 ? 0 : d / per;
+                    pick<CS>(dst, owner)[d - owner * per] = v;
+                } else {
+                    bad = true;
+                }
+            });
+        }
+        if constexpr (CS == 1)  // the placements are read next by the bulk-copy engine
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        cluster_barrier<CS>();  // every placement has landed
+        const int64_t q0 = l0 + static_cast<int64_t>(r) * per;
+        if (CS == 1 && mine >= 2 && (reinterpret_cast<uintptr_t>(qL + q0) & 15u) == 0) {
+            if (threadIdx.x == 0)
+                bulk_store(qL + q0, out, static_cast<uint32_t>(mine & ~1) * 8u);
+            if ((mine & 1) && threadIdx.x == 32)
+                qL[q0 + mine - 1] = out[mine - 1];
+        } else {
+            for (int32_t i = threadIdx.x; i < mine; i += kT)
+                qL[q0 + i] = out[i];
+        }
+        if (bad && (threadIdx.x == 0 || ok))
+            flag(a.err);
+        // the bulk store has read `out` (thread 0 waited for it) and the
+        // peers are done with this slice before it is zeroed again
+        cluster_barrier<CS>();
     }
-    if constexpr (CS == 1)  // the placements are read next by the bulk-copy engine
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    cluster_barrier<CS>();  // every placement has landed
-    const int64_t q0 = l0 + static_cast<int64_t>(r) * per;
-    if (CS == 1 && mine >= 2 && (reinterpret_cast<uintptr_t>(qL + q0) & 15u) == 0) {
-        if (threadIdx.x == 0)
-            bulk_store(qL + q0, out, static_cast<uint32_t>(mine & ~1) * 8u);
-        if ((mine & 1) && threadIdx.x == 32)
-            qL[q0 + mine - 1] = out[mine - 1];
-    } else {
-        for (int32_t i = threadIdx.x; i < mine; i += kT)
-            qL[q0 + i] = out[i];
-    }
-    if (bad && (threadIdx.x == 0 || ok))
-        flag(a.err);
 }
 
 // ---------------------------------------------------------------- gather
-// One cluster per tile of CS * g_tile_len locals.
+// One cluster per tile of CS * g_tile_len locals; a grid with fewer
+// clusters than tiles loops over tiles (persistent).
 template <int CS>
 __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const double *__restrict__ qL)
 {
@@ -831,52 +866,54 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
     double *vals = reinterpret_cast<double *>(smem);
     int64_t *runs = reinterpret_cast<int64_t *>(vals + a.g_tile_len);
     int32_t *runD = reinterpret_cast<int32_t *>(runs + a.g_nbuckets + 1);
-    const int r = cluster_rank<CS>();
-    const int u = blockIdx.x / CS;
-    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
-        pf_gather_tile(a, u, qL);
-        if (a.pf_mode > 1 && u + a.pf_ahead < a.g_ntiles)
-            pf_gather_tile(a, u + a.pf_ahead, qL);
-    }
-    const int32_t per = a.g_tile_len;
-    const int64_t l0 = static_cast<int64_t>(u) * CS * per;
-    const int64_t rest = a.NL - l0;
-    const int32_t len = static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
-    const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
-    bool ok = len > 0 && s0 >= 0 && s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
     __shared__ uint64_t bar;
     if (threadIdx.x == 0)
         mbar_init(&bar);
     __syncthreads();
-    const int32_t m0 = ok ? min(r * per, len) : 0, m1 = ok ? min((r + 1) * per, len) : 0;
-    const bool bulk = stage_start(vals, qL + l0 + m0, m1 - m0, &bar);
-    const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
-    if (!bulk)
-        stage(vals, qL + l0 + m0, m1 - m0);
-    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
-         run_off(runs[a.g_nbuckets]) == s1 - s0;
-    ok = stage_wait(bulk, &bar) && ok;
+    const int r = cluster_rank<CS>();
+    const int step = static_cast<int>(gridDim.x) / CS;
     double *tile[CS];
     map_cluster<CS>(vals, tile);
-    cluster_barrier<CS>();
-    if (ok) {
-        const int32_t total = s1 - s0;
-        const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
-        const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
-        if (emit_runs<CS>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per, len,
-                          a.work, a.nnz))
+    StageState st;
+    for (int u = static_cast<int>(blockIdx.x) / CS; u < a.g_ntiles; u += step) {
+        const int32_t per = a.g_tile_len;
+        const int64_t l0 = static_cast<int64_t>(u) * CS * per;
+        const int64_t rest = a.NL - l0;
+        const int32_t len =
+            static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
+        const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
+        bool ok = len > 0 && s0 >= 0 && s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len && !st.broken;
+        const int32_t m0 = ok ? min(r * per, len) : 0, m1 = ok ? min((r + 1) * per, len) : 0;
+        const bool bulk = stage_start(vals, qL + l0 + m0, m1 - m0, &bar, !st.broken);
+        const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
+        if (!bulk)
+            stage(vals, qL + l0 + m0, m1 - m0);
+        ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
+             run_off(runs[a.g_nbuckets]) == s1 - s0;
+        ok = stage_done(st, bulk, &bar) && ok;
+        if (a.pf_next && pf_lane() && u + step < a.g_ntiles)
+            pf_gather_tile(a, u + step, qL);
+        cluster_barrier<CS>();
+        if (ok) {
+            const int32_t total = s1 - s0;
+            const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
+            const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
+            if (emit_runs<CS>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per, len,
+                              a.work, a.nnz))
+                flag(a.err);
+        } else if (threadIdx.x == 0) {
             flag(a.err);
-    } else if (threadIdx.x == 0) {
-        flag(a.err);
+        }
+        cluster_barrier<CS>();
     }
-    cluster_barrier<CS>();
 }
 
 // One cluster per bucket = CS consecutive sub-buckets of rows; block r
 // holds sub-bucket r, its values staged grouped by row length; it places
 // 1/CS of the bucket's work entries into the owning block, then sums its
 // rows group by group (a warp's lanes all sum rows of the same length) and
-// writes its rows of q_G in order.
+// writes its rows of q_G in order.  A grid with fewer clusters than
+// buckets loops over buckets (persistent).
 template <int CS>
 __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double *__restrict__ qG)
 {
@@ -886,154 +923,155 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
     __shared__ int32_t grpRows[kMaxRow + 1];  // rows of each length
     __shared__ int grp_bad;
     const int r = cluster_rank<CS>();
-    const int c = blockIdx.x / CS;
-    if (CS == 1 && a.pf_mode && threadIdx.x == 0) {
-        pf_gather_bucket(a, c, a.work);
-        if (a.pf_mode > 1 && c + a.pf_ahead < a.g_nbuckets)
-            pf_gather_bucket(a, c + a.pf_ahead, a.work);
-    }
-    const int MM = a.g_mmax;
-    const int64_t sb = static_cast<int64_t>(c) * CS + r;
-    // Independent loads first: the bucket's work range, this block's rows
-    // and its group table.
-    const int32_t j0 = a.g_runStart[c];
-    const int32_t j1 = a.g_runStart[static_cast<int64_t>(a.g_ntiles) * a.g_nbuckets + c];
-    const int32_t r0 = a.g_subRows[sb], r1 = a.g_subRows[sb + 1];
-    const int32_t nrows = r1 - r0;
-    bool ok = MM >= 1 && MM <= kMaxRow && r0 >= 0 && nrows >= 0 && r1 <= a.NG;
-    if (MM >= 1 && MM <= kMaxRow && threadIdx.x <= MM)
-        grp[threadIdx.x] = a.g_groupStart[sb * (MM + 1) + threadIdx.x];
-    // entry offsets of the CS sub-buckets relative to the bucket start
-    int32_t sub[CS + 1];
-    int32_t E0;
-    bool csr_ok = true;  // the plan agrees with the CSR (checked late)
-    if constexpr (CS == 1) {
-        // the bucket's work range is its CSR entry range: no dependent load
-        // before the placement; rowStarts is compared after it
-        E0 = j0;
-        sub[0] = 0;
-        sub[1] = j1 - j0;
-        ok = ok && sub[1] <= a.g_bucket_entries_max;
-        const int32_t s0 = ok ? a.rowStarts[r0] : 0, s1 = ok ? a.rowStarts[r1] : 0;
-        csr_ok = s0 == j0 && s1 == j1;
-    } else {
-        const int32_t b0 = a.g_subRows[static_cast<int64_t>(c) * CS];
-        ok = ok && b0 >= 0 && b0 <= a.NG;
-        E0 = ok ? a.rowStarts[b0] : 0;
-#pragma unroll
-        for (int j = 0; j <= CS; ++j) {
-            const int32_t row = a.g_subRows[static_cast<int64_t>(c) * CS + j];
-            ok = ok && row >= b0 && row <= a.NG;
-            sub[j] = ok ? a.rowStarts[row] - E0 : 0;
-            if (j > 0)
-                ok = ok && sub[j] >= sub[j - 1] && sub[j] - sub[j - 1] <= a.g_bucket_entries_max;
-        }
-        ok = ok && j0 == E0 && j1 == E0 + sub[CS];
-    }
-    int32_t mine0 = sub[0], mine1 = sub[1];
-#pragma unroll
-    for (int w = 1; w < CS; ++w)
-        if (r == w) {
-            mine0 = sub[w];
-            mine1 = sub[w + 1];
-        }
-    const int32_t ne = sub[CS], mine = mine1 - mine0;
-    ok = ok && E0 >= 0 && ne >= 0 && E0 + ne <= a.nnz;
-    if (threadIdx.x == 0)
-        grp_bad = 0;
+    const int step = static_cast<int>(gridDim.x) / CS;
     double *dst[CS];
     map_cluster<CS>(vals, dst);
-    cluster_barrier<CS>();  // all blocks resident; grp staged
-    if (ok && threadIdx.x == 0) {
-        // rows of length m: (grp[m] - grp[m-1]) / m
-        int bad = grp[0] != 0 || grp[MM] != mine;
-        int32_t acc = 0;
-        for (int m = 1; m <= MM; ++m) {
-            const int32_t len = grp[m] - grp[m - 1];
-            bad |= len < 0 || len % m != 0;
-            grpRows[m] = len / m;
-            acc += len / m;
-        }
-        bad |= acc > nrows;
-        grp_bad = bad;
-    }
-    bool bad = false;
-    if (ok) {
-        const int32_t jb = static_cast<int32_t>(static_cast<int64_t>(ne) * r / CS);
-        const int32_t je = static_cast<int32_t>(static_cast<int64_t>(ne) * (r + 1) / CS);
-        stream_entries<CS == 1 ? kU : 6>(a.g_pos + E0, a.work + E0, jb, je, [&](uint32_t p, double v) {
-            if (p < static_cast<uint32_t>(ne)) {
-                int owner = 0;
-                int32_t base = sub[0];
+    const int MM = a.g_mmax;
+    for (int c = static_cast<int>(blockIdx.x) / CS; c < a.g_nbuckets; c += step) {
+        if (a.pf_next && pf_lane() && c + step < a.g_nbuckets)
+            pf_gather_bucket(a, c + step, a.work);
+        const int64_t sb = static_cast<int64_t>(c) * CS + r;
+        // Independent loads first: the bucket's work range, this block's
+        // rows and its group table.
+        const int32_t j0 = a.g_runStart[c];
+        const int32_t j1 = a.g_runStart[static_cast<int64_t>(a.g_ntiles) * a.g_nbuckets + c];
+        const int32_t r0 = a.g_subRows[sb], r1 = a.g_subRows[sb + 1];
+        const int32_t nrows = r1 - r0;
+        bool ok = MM >= 1 && MM <= kMaxRow && r0 >= 0 && nrows >= 0 && r1 <= a.NG;
+        if (MM >= 1 && MM <= kMaxRow && threadIdx.x <= MM)
+            grp[threadIdx.x] = a.g_groupStart[sb * (MM + 1) + threadIdx.x];
+        // entry offsets of the CS sub-buckets relative to the bucket start
+        int32_t sub[CS + 1];
+        int32_t E0;
+        bool csr_ok = true;  // the plan agrees with the CSR (checked late)
+        if constexpr (CS == 1) {
+            // the bucket's work range is its CSR entry range: no dependent
+            // load before the placement; rowStarts is compared after it
+            E0 = j0;
+            sub[0] = 0;
+            sub[1] = j1 - j0;
+            ok = ok && sub[1] <= a.g_bucket_entries_max;
+            const int32_t s0 = ok ? a.rowStarts[r0] : 0, s1 = ok ? a.rowStarts[r1] : 0;
+            csr_ok = s0 == j0 && s1 == j1;
+        } else {
+            const int32_t b0 = a.g_subRows[static_cast<int64_t>(c) * CS];
+            ok = ok && b0 >= 0 && b0 <= a.NG;
+            E0 = ok ? a.rowStarts[b0] : 0;
 #pragma unroll
-                for (int w = 1; w < CS; ++w) {
-                    owner += p >= static_cast<uint32_t>(sub[w]);
-                    base = p >= static_cast<uint32_t>(sub[w]) ? sub[w] : base;
-                }
-                pick<CS>(dst, owner)[p - base] = v;
-            } else {
-                bad = true;
+            for (int j = 0; j <= CS; ++j) {
+                const int32_t row = a.g_subRows[static_cast<int64_t>(c) * CS + j];
+                ok = ok && row >= b0 && row <= a.NG;
+                sub[j] = ok ? a.rowStarts[row] - E0 : 0;
+                if (j > 0)
+                    ok = ok && sub[j] >= sub[j - 1] && sub[j] - sub[j - 1] <= a.g_bucket_entries_max;
             }
-        });
-    }
-    // the first rows' staged positions, in flight during the row sums
-    constexpr int kRP = 16;
-    uint16_t rp[kRP];
-#pragma unroll
-    for (int q = 0; q < kRP; ++q) {
-        const int32_t k = threadIdx.x + q * kT;
-        rp[q] = ok && k < nrows ? ld_u16(a.g_rowPos + r0 + k) : 0;
-    }
-    cluster_barrier<CS>();  // every placement has landed; grpRows ready
-    const bool go = ok && grp_bad == 0 && csr_ok;
-    if (go) {
-        // sums group by group, in place into each row's first slot; a group
-        // is column-major, so the lanes of a warp read consecutive words
-        // (a one-entry row is its own sum)
-        for (int m = 2; m <= MM; ++m) {
-            const int32_t R = grpRows[m], base = grp[m - 1];
-            for (int32_t q = threadIdx.x; q < R; q += kT)
-                vals[base + q] = row_sum(vals + base + q, m, R);
+            ok = ok && j0 == E0 && j1 == E0 + sub[CS];
         }
-    }
-    __syncthreads();
-    if (go) {
-        // q_G[row] = the row's sum, +0.0 for a row without entries (0xFFFF)
+        int32_t mine0 = sub[0], mine1 = sub[1];
+#pragma unroll
+        for (int w = 1; w < CS; ++w)
+            if (r == w) {
+                mine0 = sub[w];
+                mine1 = sub[w + 1];
+            }
+        const int32_t ne = sub[CS], mine = mine1 - mine0;
+        ok = ok && E0 >= 0 && ne >= 0 && E0 + ne <= a.nnz;
+        if (threadIdx.x == 0)
+            grp_bad = 0;
+        cluster_barrier<CS>();  // all blocks resident; grp staged
+        if (ok && threadIdx.x == 0) {
+            // rows of length m: (grp[m] - grp[m-1]) / m
+            int bad = grp[0] != 0 || grp[MM] != mine;
+            int32_t acc = 0;
+            for (int m = 1; m <= MM; ++m) {
+                const int32_t len = grp[m] - grp[m - 1];
+                bad |= len < 0 || len % m != 0;
+                grpRows[m] = len / m;
+                acc += len / m;
+            }
+            bad |= acc > nrows;
+            grp_bad = bad;
+        }
+        bool bad = false;
+        if (ok) {
+            const int32_t jb = static_cast<int32_t>(static_cast<int64_t>(ne) * r / CS);
+            const int32_t je = static_cast<int32_t>(static_cast<int64_t>(ne) * (r + 1) / CS);
+            stream_entries<CS == 1 ? kU : 6>(a.g_pos + E0, a.work + E0, jb, je,
+                                             [&](uint32_t p, double v) {
+                if (p < static_cast<uint32_t>(ne)) {
+                    int owner = 0;
+                    int32_t base = sub[0];
+#pragma unroll
+                    for (int w = 1; w < CS; ++w) {
+                        owner += p >= static_cast<uint32_t>(sub[w]);
+                        base = p >= static_cast<uint32_t>(sub[w]) ? sub[w] : base;
+                    }
+                    pick<CS>(dst, owner)[p - base] = v;
+                } else {
+                    bad = true;
+                }
+            });
+        }
+        // the first rows' staged positions, in flight during the row sums
+        constexpr int kRP = 16;
+        uint16_t rp[kRP];
 #pragma unroll
         for (int q = 0; q < kRP; ++q) {
             const int32_t k = threadIdx.x + q * kT;
-            if (k < nrows) {
-                double v = 0.0;
-                if (rp[q] != 0xFFFF) {
-                    if (rp[q] < mine)
-                        v = plus_zero(vals[rp[q]]);
-                    else
-                        bad = true;
-                }
-                qG[r0 + k] = v;
+            rp[q] = ok && k < nrows ? ld_u16(a.g_rowPos + r0 + k) : 0;
+        }
+        cluster_barrier<CS>();  // every placement has landed; grpRows ready
+        const bool go = ok && grp_bad == 0 && csr_ok;
+        if (go) {
+            // sums group by group, in place into each row's first slot; a
+            // group is column-major, so the lanes of a warp read
+            // consecutive words (a one-entry row is its own sum)
+            for (int m = 2; m <= MM; ++m) {
+                const int32_t R = grpRows[m], base = grp[m - 1];
+                for (int32_t q = threadIdx.x; q < R; q += kT)
+                    vals[base + q] = row_sum(vals + base + q, m, R);
             }
         }
-        for (int32_t k0 = kRP * kT + threadIdx.x; k0 < nrows; k0 += kU * kT) {
-            uint16_t p[kU];
+        __syncthreads();
+        if (go) {
+            // q_G[row] = the row's sum, +0.0 for a row without entries (0xFFFF)
 #pragma unroll
-            for (int q = 0; q < kU; ++q)
-                p[q] = k0 + q * kT < nrows ? ld_u16(a.g_rowPos + r0 + k0 + q * kT) : 0;
-#pragma unroll
-            for (int q = 0; q < kU; ++q)
-                if (k0 + q * kT < nrows) {
+            for (int q = 0; q < kRP; ++q) {
+                const int32_t k = threadIdx.x + q * kT;
+                if (k < nrows) {
                     double v = 0.0;
-                    if (p[q] != 0xFFFF) {
-                        if (p[q] < mine)
-                            v = plus_zero(vals[p[q]]);
+                    if (rp[q] != 0xFFFF) {
+                        if (rp[q] < mine)
+                            v = plus_zero(vals[rp[q]]);
                         else
                             bad = true;
                     }
-                    qG[r0 + k0 + q * kT] = v;
+                    qG[r0 + k] = v;
                 }
+            }
+            for (int32_t k0 = kRP * kT + threadIdx.x; k0 < nrows; k0 += kU * kT) {
+                uint16_t p[kU];
+#pragma unroll
+                for (int q = 0; q < kU; ++q)
+                    p[q] = k0 + q * kT < nrows ? ld_u16(a.g_rowPos + r0 + k0 + q * kT) : 0;
+#pragma unroll
+                for (int q = 0; q < kU; ++q)
+                    if (k0 + q * kT < nrows) {
+                        double v = 0.0;
+                        if (p[q] != 0xFFFF) {
+                            if (p[q] < mine)
+                                v = plus_zero(vals[p[q]]);
+                            else
+                                bad = true;
+                        }
+                        qG[r0 + k0 + q * kT] = v;
+                    }
+            }
         }
+        if (bad || (!go && threadIdx.x == 0))
+            flag(a.err);
+        cluster_barrier<CS>();  // vals, grp and grpRows are rewritten next
     }
-    if (bad || (!go && threadIdx.x == 0))
-        flag(a.err);
 }
 
 // ------------------------------------------- fused Z^T diag(d) Z (pass 2 + 1)
@@ -1043,7 +1081,7 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
 // `ws`) in shared memory -- that is q_L = Z x on the range, masked locals
 // +0.0 --, multiplies by d_L (skipped for dL == nullptr: the identity local
 // operator), and emits gather tile u's runs into `wg` directly, so q_L
-// never reaches HBM.
+// never reaches HBM.  A grid with fewer blocks than ranges loops over them.
 __global__ void __launch_bounds__(kT, 1)
     fused_diag_kernel(PlanArgs a, const double *__restrict__ ws, const double *__restrict__ dL,
                       double *__restrict__ wg)
@@ -1052,67 +1090,68 @@ __global__ void __launch_bounds__(kT, 1)
     double *vals = reinterpret_cast<double *>(smem);
     int64_t *runs = reinterpret_cast<int64_t *>(vals + a.g_tile_len);
     int32_t *runD = reinterpret_cast<int32_t *>(runs + a.g_nbuckets + 1);
-    const int u = blockIdx.x;
-    if (a.pf_mode && threadIdx.x == 0) {
-        for (int k = 0; k < (a.pf_mode > 1 ? 2 : 1); ++k) {
-            const int v = u + k * a.pf_ahead;
-            if (v >= a.g_ntiles)
-                break;
+    const int step = static_cast<int>(gridDim.x);
+    for (int u = static_cast<int>(blockIdx.x); u < a.g_ntiles; u += step) {
+        if (a.pf_next && pf_lane() && u + step < a.g_ntiles) {
+            const int v = u + step;
             pf_scatter_bucket(a, v, ws);
-            int64_t d0 = static_cast<int64_t>(v) * a.g_tile_len, d1 = d0 + a.g_tile_len;
-            if (clamp_range(d0, d1, a.NL))
-                prefetch_l2(dL + d0, 8 * (d1 - d0));
+            if (dL) {
+                int64_t d0 = static_cast<int64_t>(v) * a.g_tile_len, d1 = d0 + a.g_tile_len;
+                if (clamp_range(d0, d1, a.NL))
+                    prefetch_l2(dL + d0, 8 * (d1 - d0));
+            }
             int64_t s0 = a.g_tileSlot[v], s1 = a.g_tileSlot[v + 1];
             if (clamp_range(s0, s1, a.nnz))
                 prefetch_l2(a.g_src + s0, 2 * (s1 - s0));
             prefetch_l2(a.g_runStart + static_cast<int64_t>(v) * a.g_nbuckets, 8ll * a.g_nbuckets);
         }
-    }
-    const int64_t l0 = static_cast<int64_t>(u) * a.g_tile_len;
-    const int32_t len = static_cast<int32_t>(a.NL - l0 < a.g_tile_len ? a.NL - l0 : a.g_tile_len);
-    const int32_t j0 = a.s_runStart[u];
-    const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + u];
-    const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
-    bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len && s0 >= 0 &&
-              s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
-    if (!(ok && j1 - j0 == len))  // (no masked local: every slot is placed)
-        for (int32_t i = threadIdx.x; i < len; i += kT)
-            vals[i] = 0.0;
-    const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
-    __syncthreads();  // zeroed
-    bool bad = false;
-    if (ok) {
-        stream_entries<6, true>(a.s_dst, ws, j0, j1, [&](uint32_t d, double v) {
-            if (d < static_cast<uint32_t>(len))
-                vals[d] = v;
-            else
-                bad = true;
-        });
-    }
-    // (commit_runs begins with a barrier: the placements are complete after it)
-    ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
-         run_off(runs[a.g_nbuckets]) == s1 - s0;
-    if (ok && dL) {
-        for (int32_t i0 = threadIdx.x; i0 < len; i0 += kU * kT) {
-            double w[kU];
-#pragma unroll
-            for (int q = 0; q < kU; ++q)
-                w[q] = i0 + q * kT < len ? ld_seq(dL + l0 + i0 + q * kT) : 0.0;
-#pragma unroll
-            for (int q = 0; q < kU; ++q)
-                if (i0 + q * kT < len)
-                    vals[i0 + q * kT] = __dmul_rn(w[q], vals[i0 + q * kT]);
+        const int64_t l0 = static_cast<int64_t>(u) * a.g_tile_len;
+        const int32_t len = static_cast<int32_t>(a.NL - l0 < a.g_tile_len ? a.NL - l0 : a.g_tile_len);
+        const int32_t j0 = a.s_runStart[u];
+        const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + u];
+        const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
+        bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len && s0 >= 0 &&
+                  s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
+        if (!(ok && j1 - j0 == len))  // (no masked local: every slot is placed)
+            for (int32_t i = threadIdx.x; i < len; i += kT)
+                vals[i] = 0.0;
+        const RunFetch rf = fetch_runs(a.g_runStart, u, a.g_nbuckets);
+        __syncthreads();  // zeroed
+        bool bad = false;
+        if (ok) {
+            stream_entries<6, true>(a.s_dst, ws, j0, j1, [&](uint32_t d, double v) {
+                if (d < static_cast<uint32_t>(len))
+                    vals[d] = v;
+                else
+                    bad = true;
+            });
         }
+        // (commit_runs begins with a barrier: the placements are complete after it)
+        ok = commit_runs(rf, a.g_runStart, u, a.g_nbuckets, a.nnz, runs, runD) && ok &&
+             run_off(runs[a.g_nbuckets]) == s1 - s0;
+        if (ok && dL) {
+            for (int32_t i0 = threadIdx.x; i0 < len; i0 += kU * kT) {
+                double w[kU];
+#pragma unroll
+                for (int q = 0; q < kU; ++q)
+                    w[q] = i0 + q * kT < len ? ld_seq(dL + l0 + i0 + q * kT) : 0.0;
+#pragma unroll
+                for (int q = 0; q < kU; ++q)
+                    if (i0 + q * kT < len)
+                        vals[i0 + q * kT] = __dmul_rn(w[q], vals[i0 + q * kT]);
+            }
+        }
+        __syncthreads();  // scaled tile ready
+        if (ok) {
+            double *tile[1] = {vals};
+            if (emit_runs<1>(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, tile, len, len, wg,
+                             a.nnz))
+                bad = true;
+        }
+        if (bad || (!ok && threadIdx.x == 0))
+            flag(a.err);
+        __syncthreads();  // vals and the run tables are rewritten next
     }
-    __syncthreads();  // scaled tile ready
-    if (ok) {
-        double *tile[1] = {vals};
-        if (emit_runs<1>(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, tile, len, len, wg,
-                         a.nnz))
-            bad = true;
-    }
-    if (bad || (!ok && threadIdx.x == 0))
-        flag(a.err);
 }
 
 int64_t smem_s1(const bs_plan_dev *p) { return 8ll * p->s_tile_rows + 8ll * (p->s_nbuckets + 1) + 4ll * p->s_nbuckets; }
@@ -1122,10 +1161,18 @@ int64_t smem_g2(const bs_plan_dev *p) { return 8ll * p->g_bucket_entries_max + 4
 
 constexpr int64_t kSmemMax = 232448;
 
+// Launches `kernel` over `items` tiles or buckets: one cluster of `cs`
+// blocks per item, or, with the context's persistent setting, at most one
+// cluster per `cs` SMs, each looping over its items.
 template <class... KArgs, class... Args>
-int launch(bs_ctx *ctx, const char *name, void (*kernel)(KArgs...), int cs, int64_t clusters,
+int launch(bs_ctx *ctx, const char *name, void (*kernel)(KArgs...), int cs, int64_t items,
            int64_t smem, cudaStream_t s, Args... args)
 {
+    int64_t clusters = items;
+    if (ctx->tune.persist) {
+        const int64_t cap = ctx->sms / cs > 0 ? ctx->sms / cs : 1;
+        clusters = items < cap ? items : cap;
+    }
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess)
@@ -1218,8 +1265,7 @@ PlanArgs make_args(const bs_ctx *ctx, const bs_gs_dev *t)
     a.g_rowPos = p->g_rowPos;
     a.work = p->work;
     a.err = ctx->dev_err;
-    a.pf_mode = ctx->tune.l2_prefetch;
-    a.pf_ahead = ctx->sms;
+    a.pf_next = ctx->tune.persist && ctx->tune.l2_prefetch;
     return a;
 }
 

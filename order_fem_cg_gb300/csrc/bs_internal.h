@@ -20,8 +20,10 @@ struct bs_tune {
     int reduce_blocks_per_sm;  // BS3-BS5 grid = SMs x this (capped by kMaxReduceBlocks)
     int scatter_blocks_per_sm; // BS7 grid = SMs x this
     int vec_width;             // widest vector in doubles: 4 (32 B), 2 (16 B) or 1
-    int l2_prefetch;           // two-pass kernels: 0 none (default: measured fastest),
-                               // 1 own inputs, 2 also the inputs of the block one wave ahead
+    int persist;               // two-pass kernels: 1 one block (cluster) per SM looping over
+                               // tiles/buckets, 0 one block per tile/bucket
+    int l2_prefetch;           // persistent two-pass kernels: 1 prefetch each block's next
+                               // tile/bucket into L2 while it works on the current one
     int small_onepass;         // 1: one-pass gather/scatter for L2-sized vectors even with a
                                // plan (bs_gather / bs_scatter); 0: always the plan
 };

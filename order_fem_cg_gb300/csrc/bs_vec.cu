@@ -23,7 +23,6 @@
 //    finish of the last warp.
 #include <cuda_runtime.h>
 
-#include <mutex>
 
 #include "bs_internal.h"
 
@@ -482,24 +481,6 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// ------------------------------------------------------ binary64 FMA probe
-__global__ void __launch_bounds__(kThreads) probe_dfma_kernel(int64_t iters, double *sink)
-{
-    double a[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        a[k] = 1.0 + (threadIdx.x + 37 * k) * 1e-9;
-    const double m = 0.99999999, c = 1e-9;
-    for (int64_t i = 0; i < iters; ++i) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            a[k] = __fma_rn(a[k], m, c);
-    }
-    double s = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-    if (s == -1.0)  // never true; keeps the chains alive
-        *sink = s;
-}
-
 // ------------------------------------------------------------- host side
 
 // How a length-n operation over the given operands is split into a scalar
@@ -762,36 +743,21 @@ extern "C" int bs_cg_update(bs_ctx *ctx, int64_t n, const double *alpha_num_dev,
     return BS_OK;
 }
 
-extern "C" int bs_probe_dfma(bs_ctx *ctx, int blocks_per_sm, int64_t iters, double *sink_dev,
-                             void *stream)
-{
-    if (!ctx)
-        return BS_EINVAL;
-    if (blocks_per_sm < 1 || blocks_per_sm > 64 || iters < 0 || !sink_dev)
-        return bs_set_error(ctx, BS_EINVAL, "bs_probe_dfma: bad argument");
-    if (int st = bs_check_device(ctx))
-        return st;
-    probe_dfma_kernel<<<ctx->sms * blocks_per_sm, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        iters, sink_dev);
-    BS_LAUNCH_CHECK(ctx, "probe_dfma_kernel");
-    return BS_OK;
-}
-
 // ---------------------------------------------------------------------------
 // Allocation-free inner product.
 //
-// Some callers cannot call cudaMalloc: code that runs inside a memory
-// allocator's own hooks, a host callback, or an embedding runtime that owns
-// every device allocation and forbids others.  They cannot create a bs_ctx
-// either, since a context allocates its reduction workspace.  bs_dot_noalloc
-// runs the same BS4 kernel as bs_dot but keeps the per-block partial sums
-// and the completion counter in the fixed array below, which every GPU that
-// loads this library holds until the process exits.
+// Some callers cannot call cudaMalloc: code that runs inside a device-memory
+// allocator's own hooks (where allocating would recurse into the allocator),
+// or an embedding runtime that owns every device allocation and forbids
+// others.  They cannot create a bs_ctx either, since a context allocates its
+// reduction workspace.  bs_dot_noalloc runs the same BS4 kernel as bs_dot
+// but keeps the per-block partial sums and the completion counter in the
+// fixed array below, which every GPU that loads this library holds until
+// the process exits.
 namespace {
 constexpr int kNoAllocMaxBlocks = 1024;  // partial sums the array can hold
 constexpr size_t kNoAllocCounterOffset = kNoAllocMaxBlocks * sizeof(double);
 constexpr size_t kNoAllocScratchBytes = kNoAllocCounterOffset + 256;
-constexpr int kNoAllocMaxDevices = 64;
 constexpr int kNoAllocBlocksPerSm = 4;
 } // namespace
 
@@ -799,34 +765,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 namespace {
 
-std::mutex g_noalloc_mutex;
-void *g_noalloc_addr[kNoAllocMaxDevices];
-int g_noalloc_sms[kNoAllocMaxDevices];
-
-// Device address of the scratch array and the SM count of the current
-// device, looked up once per device (the first call on a device does it).
-int noalloc_setup(int *dev_out, unsigned char **scratch, int *sms)
+// Device address of the scratch array on the current device and that
+// device's SM count.  The address is looked up on every call (a host-side
+// lookup once the module is loaded, no allocation): a cached address could
+// outlive the context that the array lives in (cudaDeviceReset, a new
+// primary context), and a kernel given it would write to unmapped memory.
+int noalloc_setup(unsigned char **scratch, int *sms)
 {
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
         cudaGetLastError();
         return BS_ECUDA;
     }
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
-        void *p = nullptr;
-        int n_sms = 0;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
-            cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return BS_ECUDA;
-        }
-        g_noalloc_sms[dev] = n_sms;
-        g_noalloc_addr[dev] = p;
+    void *p = nullptr;
+    int n_sms = 0;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
+        cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n_sms < 1) {
+        cudaGetLastError();  // this call's own error (none was pending on entry)
+        return BS_ECUDA;
     }
-    *dev_out = dev;
-    *scratch = static_cast<unsigned char *>(g_noalloc_addr[dev]);
-    *sms = g_noalloc_sms[dev];
+    *scratch = static_cast<unsigned char *>(p);
+    *sms = n_sms;
     return BS_OK;
 }
 
@@ -839,13 +799,22 @@ extern "C" int bs_dot_noalloc(int64_t n, const double *x, const double *y, doubl
         return BS_EINVAL;
     if (!aligned8(out_dev) || (n > 0 && (!aligned8(x) || !aligned8(y))))
         return BS_EINVAL;
-    int dev = 0, sms = 0;
+    // An error left pending by the caller's earlier work stays theirs: report
+    // it, launch nothing and do not clear it.  Past this point any error the
+    // runtime reports is this call's own.
+    if (cudaPeekAtLastError() != cudaSuccess)
+        return BS_ECUDA;
+    int sms = 0;
     unsigned char *scratch = nullptr;
-    if (int st = noalloc_setup(&dev, &scratch, &sms))
+    if (int st = noalloc_setup(&scratch, &sms))
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (n == 0)
-        return cudaMemsetAsync(out_dev, 0, sizeof(double), s) == cudaSuccess ? BS_OK : BS_ECUDA;
+    if (n == 0) {
+        if (cudaMemsetAsync(out_dev, 0, sizeof(double), s) == cudaSuccess)
+            return BS_OK;
+        cudaGetLastError();
+        return BS_ECUDA;
+    }
     const void *ps[2] = {x, y};
     const Plan pl = make_plan(n, 4, ps, 2);
     const int64_t need = ((pl.nv + kReduceUnroll - 1) / kReduceUnroll + kThreads - 1) / kThreads;
@@ -856,8 +825,10 @@ extern "C" int bs_dot_noalloc(int64_t n, const double *x, const double *y, doubl
         return BS_EINVAL;  // the device wants more partial sums than the array holds
     unsigned int *counter = reinterpret_cast<unsigned int *>(scratch + kNoAllocCounterOffset);
     // The array keeps the previous call's contents; the counter must start at 0.
-    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess)
+    if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), s) != cudaSuccess) {
+        cudaGetLastError();
         return BS_ECUDA;
+    }
     const RedOut o{reinterpret_cast<double *>(scratch), counter, out_dev};
     switch (pl.V) {
     case 4: launch_dot<4, true>(static_cast<int>(grid), s, x, y, pl, o); break;
