@@ -165,18 +165,27 @@ __device__ __forceinline__ void finish_reduction(double v, const RedOut &o)
 // GB300 runs binary64 fma/add at ~1.6 per clock per SM, so a sum of
 // squares with one fma per element is bound by the FP64 pipe below HBM
 // speed.  SqAcc forms x^2 and sums it on the FP32 and integer pipes:
-//   |x| = xh + xl with xh the leading 24 significant bits (a float, exact)
-//   and xl the next 23 bits (exact float; the last 6 bits are dropped,
-//   an error below 2^-46 |x|), built with integer and FP32 operations only
-//   (on this part int<->float conversions are as scarce as FP64 math);
+//   |x| = xh + xl + dx with xh the leading 24 significant bits (a float,
+//   exact), xl the next 23 bits (exact float) and dx the last 6 bits,
+//   dropped: 0 <= dx < 2^-46 |x|; built with integer and FP32 operations
+//   only (on this part int<->float conversions are as scarce as FP64 math);
 //   x^2 ~= xh^2 + (2 xh xl + xl^2), xh^2 exact as p + e (TwoProduct by
-//   fmaf); p is added to a float-float sum (s, c) by TwoSum, the small
-//   terms to c.  Every flush (8 elements) moves (s, c) into a binary64 total
-//   with an exact float->double conversion done on the integer pipe.
-// Per element the relative error is <= ~2^-45; per 8-element chunk the
-// float accumulation adds <= ~2^-40; all terms are >= 0, so the total
-// stays within 1e-12 relative.  |x| outside [2^-40, 2^41) (subnormal,
-// tiny, huge, inf, NaN) goes through a separate binary64 fma sum instead.
+//   fmaf); p is added to a float-float sum (s, c) by TwoSum (exact), the
+//   small terms q = e + 2 xh xl + xl^2 (two fmaf roundings) to c.  Every
+//   chunk of at most 8 elements is flushed: (s, c) move into a binary64
+//   total through an exact float->double conversion on the integer pipe.
+// Worst case, for a chunk with exact sum S of squares (all terms >= 0):
+//   dropped bits: x^2 underestimated by <= 2^-45 x^2;
+//   q's two roundings: <= 2 * 2^-24 * 1.25 * 2^-22 x^2 = 1.25 * 2^-45 x^2;
+//   c: every term t_j = err_j + q_j has |err_j| <= 2^-24 S (TwoSum's exact
+//   rounding error of s) and sum |q_j| <= 1.25 * 2^-22 S, so |c| <=
+//   (k 2^-24 + 1.25 * 2^-22) S = 3.25 * 2^-22 S for k = 8, and its k + k
+//   float roundings add <= 2^-24 (1 + k) * 3.25 * 2^-22 S = 29.25 * 2^-46 S;
+//   in all <= 2.25 * 2^-45 S + 29.25 * 2^-46 S < 4.8e-13 S, plus the binary64
+//   flushes and the fixed reduction tree (2^-53 per addition).  So the
+//   total is within 5e-13 relative of the exact sum of squares.  |x|
+//   outside [2^-40, 2^41) (subnormal, tiny, huge, inf, NaN) goes through a
+//   separate binary64 fma sum instead.
 constexpr uint32_t kSqExpLo = 1023 - 40, kSqExpHi = 1023 + 40;
 
 __device__ __forceinline__ double float_to_double_exact(float f)
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const double *__restrict_
                     c[u] = ld_stream<V>(yv + (b + u * stride) * V);
             }
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
+        for (int u = 0; u < UNROLL; ++u) {
             if (b + u * stride < nv) {
 #pragma unroll
                 for (int k = 0; k < V; ++k) {
@@ -378,7 +387,11 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const double *__restrict_
                         sq.add(a[u].v[k], pending);
                 }
             }
-        if (!DOT)
+            // chunks of at most 8 squares (the accumulator's error bound)
+            if (!DOT && ((u + 1) * V) % 8 == 0)
+                sq.flush();
+        }
+        if (!DOT && (UNROLL * V) % 8 != 0)
             sq.flush();
     }
     if (gid < h + t) {

@@ -457,6 +457,62 @@ def test_fused_residual_wide_exponent_range():
     assert bits_equal(host(rd), ro) and rel_close(rr, rro)
 
 
+def _all_low_bits(x):
+    """x with the 29 low fraction bits set: the 6 bits the float-float split
+    drops, and the 23 it keeps in xl, are all ones."""
+    b = np.abs(x).view(np.uint64) | np.uint64((1 << 29) - 1)
+    return b.view(np.float64)
+
+
+def worst_case_vectors(n):
+    """Inputs that push the float-float sum of squares to its error bound:
+    one sign, every value with its low fraction bits all ones (the dropped
+    bits are maximal, so every square is under-estimated the same way), and
+    8-element chunks built so that each float addition into s rounds with a
+    large error: one dominant term then seven terms 2^-12 smaller in value
+    (2^-24 in square, half an ulp of s), the same pattern reversed, and all
+    terms equal to the largest double below 2."""
+    top = np.nextafter(2.0, 0.0)
+    equal = np.full(n, top)
+    pat = np.empty(8)
+    pat[0] = top
+    pat[1:] = np.ldexp(top, -12)
+    lead = np.tile(pat, n // 8 + 1)[:n]
+    trail = np.tile(pat[::-1], n // 8 + 1)[:n]
+    rnd = _all_low_bits(0.5 + 0.5 * (gen.uniform_pm1(71, 1, n) + 1.0) / 2.0)
+    return {"equal": equal, "lead": lead, "trail": trail, "random_low_bits": rnd}
+
+
+def test_norm_worst_case_at_2_27():
+    """n = 2^27 (the sweep's largest size): every worst-case pattern within
+    1e-12 of the oracle's Dot2 sum (the derived bound is 5e-13)."""
+    n = 1 << 27
+    for name, x in worst_case_vectors(n).items():
+        xd = dev(x)
+        got = host(bs.bs_norm(xd))[0]
+        ref = oracle.norm(x)
+        assert abs(got - ref) <= 1e-12 * ref, (name, got, ref, (got - ref) / ref)
+        del xd
+        torch.cuda.empty_cache()
+
+
+def test_fused_residual_worst_case_at_2_27():
+    """BS5's r.r uses the same accumulator: alpha = 0 keeps r bit for bit, so
+    r.r is the sum of squares of the worst-case patterns."""
+    n = 1 << 27
+    pats = worst_case_vectors(n)
+    p = torch.zeros(n, dtype=torch.float64, device=DEV)
+    Ap = torch.zeros(n, dtype=torch.float64, device=DEV)
+    x = torch.zeros(n, dtype=torch.float64, device=DEV)
+    for name in ("equal", "lead", "random_low_bits"):
+        r = dev(pats[name])
+        rr = host(bs.bs_cg_update(p, Ap, x, r, alpha=0.0))[0]
+        ref = oracle.norm(pats[name])
+        assert abs(rr - ref) <= 1e-12 * ref, (name, rr, ref, (rr - ref) / ref)
+        del r
+        torch.cuda.empty_cache()
+
+
 def test_norm_non_finite():
     x = gen.uniform_pm1(3, 3, 5000)
     x[1234] = np.inf

@@ -675,3 +675,49 @@ def test_planted_cg_mistakes_are_caught(which):
 
 def test_cg_mutant_harness_without_mistake_passes():
     _check_cg(_cg_mutant("none"), iters=6)
+
+
+# ----------------------------------------------------------------------------
+# One CG iteration's streaming sequence (identity local operator)
+# ----------------------------------------------------------------------------
+
+def test_cg_sequence_zero_denominator_keeps_x_and_r():
+    """p = 0 makes p.Ap = 0; the reading takes alpha = 0 there (a vanishing
+    p.Ap occurs only at an exact solution), so x and r come back bit for bit
+    and both r.r sums are the exact sum of squares (dyadic r)."""
+    cfg, _, _, ids = mesh((3, 3))
+    NG = cfg.NG
+    pG = np.zeros(NG)
+    xG = gen.uniform_pm1(61, 1, NG)
+    rG = np.round(gen.uniform_pm1(61, 2, NG) * 64) / 8   # multiples of 1/8, |r| <= 8
+    rG[rG == 0] = 0.125                                    # no signed zeros
+    out = oracle.cg_sequence(ids, pG, xG, rG, rr=3.5)
+    assert out["pAp"] == 0.0 and out["alpha"] == 0.0
+    assert np.array_equal(out["x"].view(np.uint64), xG.view(np.uint64))
+    assert np.array_equal(out["r"].view(np.uint64), rG.view(np.uint64))
+    exact = sum(Fraction(v) ** 2 for v in rG.tolist())
+    assert Fraction(out["rr_new"]) == exact and Fraction(out["rnorm"]) == exact
+
+
+def test_cg_sequence_exact_on_small_integers():
+    """With small-integer p, x, r every step is exact: Z^T Z p = m p with m the
+    node multiplicity (counted here with bincount, not with the oracle's
+    gather), p.Ap = sum m p^2; rr = 2 p.Ap gives alpha = 2 exactly, so
+    x + 2p, r - 2 m p and their squares are exact integers."""
+    cfg, _, _, ids = mesh((3, 3))
+    NG = cfg.NG
+    m = np.bincount(ids[ids >= 0], minlength=NG).astype(np.int64)
+    pi = np.round(gen.uniform_pm1(62, 1, NG) * 7).astype(np.int64)
+    xi = np.round(gen.uniform_pm1(62, 2, NG) * 50).astype(np.int64)
+    ri = np.round(gen.uniform_pm1(62, 3, NG) * 50).astype(np.int64)
+    pAp = int(np.sum(m * pi * pi))
+    assert 0 < pAp < 2 ** 52
+    out = oracle.cg_sequence(ids, pi.astype(float), xi.astype(float), ri.astype(float),
+                             rr=float(2 * pAp))
+    assert np.array_equal(out["pL"], pi[ids].astype(float))
+    assert np.array_equal(out["ApG"], (m * pi).astype(float))
+    assert out["pAp"] == pAp and out["alpha"] == 2.0
+    assert np.array_equal(out["x"], (xi + 2 * pi).astype(float))
+    r1 = ri - 2 * m * pi
+    assert np.array_equal(out["r"], r1.astype(float))
+    assert out["rr_new"] == int(np.sum(r1 * r1)) == out["rnorm"]
