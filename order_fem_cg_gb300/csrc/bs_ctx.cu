@@ -112,6 +112,7 @@ extern "C" int bs_ctx_create(int device, bs_ctx **out)
         ctx->tune.persist = env_int("BS_TUNE_PERSIST", 0, 0, 1);
         ctx->tune.l2_prefetch = env_int("BS_TUNE_L2PF", 1, 0, 1);
         ctx->tune.small_onepass = env_int("BS_TUNE_ONEPASS", 1, 0, 1);
+        ctx->tune.tmem = env_int("BS_TUNE_TMEM", 1, 0, 1);
         if (ctx->tune.vec_width == 3)
             ctx->tune.vec_width = 2;
         if (cudaMalloc(&ctx->partials, kMaxReduceBlocks * sizeof(double)) != cudaSuccess ||

@@ -424,6 +424,35 @@ __device__ __forceinline__ double row_sum(const double *v, int n, int stride)
     return s;
 }
 
+// In-place row sums of one row-length group: the R rows of length m sit
+// column-major from `base` (entry j of row k at base + j R + k); the rows
+// k = t0, t0 + nt, ... of this thread get their sum (in row_sum's order)
+// in their first slot.  Four rows per step, so that four independent
+// addition chains are in flight (a binary64 addition's latency is tens of
+// cycles; one chain at a time leaves the FP64 pipe mostly idle).
+__device__ __forceinline__ void group_sums(double *vals, int32_t base, int m, int32_t R, int t0,
+                                           int nt)
+{
+    int32_t k = t0;
+    for (; k + 3 * nt < R; k += 4 * nt) {
+        double *v = vals + base + k;
+        double s0 = v[0], s1 = v[nt], s2 = v[2 * nt], s3 = v[3 * nt];
+        for (int j = 1; j < m; ++j) {
+            const double *w = v + j * R;
+            s0 += w[0];
+            s1 += w[nt];
+            s2 += w[2 * nt];
+            s3 += w[3 * nt];
+        }
+        v[0] = s0;
+        v[nt] = s1;
+        v[2 * nt] = s2;
+        v[3 * nt] = s3;
+    }
+    for (; k < R; k += nt)
+        vals[base + k] = row_sum(vals + base + k, m, R);
+}
+
 __device__ __forceinline__ double plus_zero(double s)
 {
     return (__double_as_longlong(s) << 1) == 0 ? 0.0 : s;
@@ -1026,11 +1055,8 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
             // sums group by group, in place into each row's first slot; a
             // group is column-major, so the lanes of a warp read
             // consecutive words (a one-entry row is its own sum)
-            for (int m = 2; m <= MM; ++m) {
-                const int32_t R = grpRows[m], base = grp[m - 1];
-                for (int32_t q = threadIdx.x; q < R; q += kT)
-                    vals[base + q] = row_sum(vals + base + q, m, R);
-            }
+            for (int m = 2; m <= MM; ++m)
+                group_sums(vals, grp[m - 1], m, grpRows[m], threadIdx.x, kT);
         }
         __syncthreads();
         if (go) {
@@ -1072,6 +1098,281 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_kernel(PlanArgs a, double
             flag(a.err);
         cluster_barrier<CS>();  // vals, grp and grpRows are rewritten next
     }
+}
+
+// ------------------------------------------- gather pass 2 with a TMEM buffer
+// The bucket kernel above holds one bucket in shared memory, so each SM
+// runs its phases back to back: place (read the work range from HBM, ~8 us
+// on the stress mesh), sum (binary64, ~3.4 us), write q_G (~4 us), and HBM
+// idles while the SM sums.  Here the SM's tensor memory (TMEM: 128 lanes x
+// 512 columns of 32 bits, 256 KB, otherwise unused by this library) holds
+// the NEXT bucket's work entries and positions: warps 16..31 stream them
+// from HBM into TMEM while warps 0..15 sum and write the current bucket,
+// and the placement then reads TMEM instead of waiting on HBM.  Persistent:
+// one block per SM, buckets blockIdx.x, blockIdx.x + gridDim.x, ...  The
+// row sums and q_G writes run on fewer warps than in the kernel above and
+// slow down somewhat; on the stress mesh a gather call still gains ~6%.
+//
+// TMEM layout of a bucket's entries j < ne: entry j sits in lane j % 128 of
+// 128-entry block j / 128; blocks are grouped by 8.  Group g's values take
+// columns 16 g .. 16 g + 15 (block 8 g + k: columns 16 g + 2 k and + 1, the
+// low and high words); its 16-bit positions take columns pc + 4 g .. + 3
+// (column pc + 4 g + i: blocks 8 g + 2 i in the low half, 8 g + 2 i + 1 in
+// the high half), entries past ne carry position 0xFFFF.  A warp reaches
+// the 32 lanes of its quarter (warp index mod 4) only, so lane 32 q + t of
+// every block is loaded, stored and read by lane t of warps in quarter q.
+constexpr int kTmGroupEntries = 1024; // 8 blocks of 128 entries
+constexpr int kTmCols = 512;
+
+__device__ __forceinline__ void tm_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tm_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Block barrier that also orders the threads' TMEM accesses around it.
+__device__ __forceinline__ void tm_sync()
+{
+    tm_fence_before();
+    __syncthreads();
+    tm_fence_after();
+}
+
+__device__ __forceinline__ void tm_st16(uint32_t addr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, "
+                 "%9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(addr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+                 "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tm_st4(uint32_t addr, const uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tm_ld16(uint32_t addr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+                 "%10, %11, %12, %13, %14, %15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tm_ld4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tm_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Work range [j0, j1) of gather bucket c (cluster 1), if the tables hold a
+// valid one that fits the staging (the checks both the loaders and the
+// placing threads apply).
+__device__ __forceinline__ bool tm_bucket_range(const PlanArgs &a, int c, int32_t &j0, int32_t &ne)
+{
+    j0 = a.g_runStart[c];
+    const int32_t j1 = a.g_runStart[static_cast<int64_t>(a.g_ntiles) * a.g_nbuckets + c];
+    ne = j1 - j0;
+    return j0 >= 0 && j1 >= j0 && j1 <= a.nnz && ne <= a.g_bucket_entries_max;
+}
+
+// Loader warp (quarter q, index i of n in its quarter): entries and
+// positions of [w, w + ne) into TMEM, groups i, i + n, ...
+__device__ __forceinline__ void tm_load(uint32_t lane_addr, int pc, const double *w,
+                                        const uint16_t *pos, int32_t ne, int q, int i, int n)
+{
+    const int lane = threadIdx.x & 31;
+    const int ng = (ne + kTmGroupEntries - 1) / kTmGroupEntries;
+    for (int g = i; g < ng; g += n) {
+        double d[8];
+        uint32_t p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int32_t j = (g * 8 + k) * 128 + q * 32 + lane;
+            d[k] = j < ne ? ld_seq(w + j) : 0.0;
+            p[k] = j < ne ? static_cast<uint32_t>(ld_u16(pos + j)) : 0xFFFFu;
+        }
+        uint32_t v[16], pk[4];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            v[2 * k] = static_cast<uint32_t>(__double2loint(d[k]));
+            v[2 * k + 1] = static_cast<uint32_t>(__double2hiint(d[k]));
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            pk[k] = p[2 * k] | (p[2 * k + 1] << 16);
+        tm_st16(lane_addr + 16u * g, v);
+        tm_st4(lane_addr + pc + 4u * g, pk);
+    }
+    tm_wait_st();
+}
+
+// Placing warp (quarter q, index i of n): vals[pos[j]] = w[j] for the
+// bucket's entries in TMEM, groups i, i + n, ...; returns true on a
+// position outside [0, ne) (skipped).
+__device__ __forceinline__ bool tm_place(uint32_t lane_addr, int pc, double *vals, int32_t ne, int q,
+                                         int i, int n)
+{
+    const int lane = threadIdx.x & 31;
+    const int ng = (ne + kTmGroupEntries - 1) / kTmGroupEntries;
+    bool bad = false;
+    for (int g = i; g < ng; g += n) {
+        uint32_t v[16], pk[4];
+        tm_ld16(lane_addr + 16u * g, v);
+        tm_ld4(lane_addr + pc + 4u * g, pk);
+        tm_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int32_t j = (g * 8 + k) * 128 + q * 32 + lane;
+            const uint32_t pos = (pk[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+            if (j < ne) {
+                if (pos < static_cast<uint32_t>(ne))
+                    vals[pos] = __hiloint2double(static_cast<int>(v[2 * k + 1]), static_cast<int>(v[2 * k]));
+                else
+                    bad = true;
+            }
+        }
+    }
+    return bad;
+}
+
+// kTmWorkers warps (a multiple of 4) sum and write; the others load.
+constexpr int kTmWorkersDefault = 20;
+template <int kTmWorkers>
+__global__ void __launch_bounds__(kT, 1) gather_bucket_tm_kernel(PlanArgs a, double *__restrict__ qG,
+                                                                 int pc)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    double *vals = reinterpret_cast<double *>(smem);
+    int32_t *grp = reinterpret_cast<int32_t *>(vals + a.g_bucket_entries_max);  // [mmax+1]
+    __shared__ int32_t grpRows[kMaxRow + 1];
+    __shared__ int grp_bad;
+    __shared__ uint32_t s_taddr;
+    const int warp = threadIdx.x >> 5, q = warp & 3;
+    const bool worker = warp < kTmWorkers;
+    const int step = static_cast<int>(gridDim.x);
+    const int MM = a.g_mmax;
+    constexpr int kW = kTmWorkers * 32;  // worker threads
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(&s_taddr))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tm_sync();
+    const uint32_t lane_addr = s_taddr + (static_cast<uint32_t>(q * 32) << 16);
+    int c = static_cast<int>(blockIdx.x);
+    if (!worker && c < a.g_nbuckets) {  // the first bucket
+        int32_t j0, ne;
+        if (tm_bucket_range(a, c, j0, ne))
+            tm_load(lane_addr, pc, a.work + j0, a.g_pos + j0, ne, q, (warp - kTmWorkers) >> 2,
+                    (32 - kTmWorkers) / 4);
+    }
+    tm_sync();
+    for (; c < a.g_nbuckets; c += step) {
+        // this bucket's entries are in TMEM
+        int32_t j0, ne;
+        const bool range_ok = tm_bucket_range(a, c, j0, ne);
+        const int32_t r0 = a.g_subRows[c], r1 = a.g_subRows[c + 1];
+        const int32_t nrows = r1 - r0;
+        bool ok = range_ok && MM >= 1 && MM <= kMaxRow && r0 >= 0 && nrows >= 0 && r1 <= a.NG;
+        if (MM >= 1 && MM <= kMaxRow && threadIdx.x <= MM)
+            grp[threadIdx.x] = a.g_groupStart[static_cast<int64_t>(c) * (MM + 1) + threadIdx.x];
+        const int32_t s0 = ok ? a.rowStarts[r0] : 0, s1 = ok ? a.rowStarts[r1] : 0;
+        const bool csr_ok = s0 == j0 && s1 == j0 + ne;  // the work range is the CSR range
+        if (threadIdx.x == 0)
+            grp_bad = 0;
+        __syncthreads();  // grp staged
+        if (ok && threadIdx.x == 0) {
+            int bad = grp[0] != 0 || grp[MM] != ne;
+            int32_t acc = 0;
+            for (int m = 1; m <= MM; ++m) {
+                const int32_t len = grp[m] - grp[m - 1];
+                bad |= len < 0 || len % m != 0;
+                grpRows[m] = len / m;
+                acc += len / m;
+            }
+            bad |= acc > nrows;
+            grp_bad = bad;
+        }
+        bool bad = ok ? tm_place(lane_addr, pc, vals, ne, q, warp >> 2, 8) : false;
+        constexpr int kRP = 16;
+        uint16_t rp[kRP];
+        if (worker) {  // the first rows' staged positions, in flight during the sums
+#pragma unroll
+            for (int k = 0; k < kRP; ++k) {
+                const int32_t row = threadIdx.x + k * kW;
+                rp[k] = ok && row < nrows ? ld_u16(a.g_rowPos + r0 + row) : 0;
+            }
+        }
+        tm_sync();  // placements landed, grpRows ready; TMEM is free
+        if (!worker) {
+            const int cn = c + step;
+            int32_t jn, nn;
+            if (cn < a.g_nbuckets && tm_bucket_range(a, cn, jn, nn))
+                tm_load(lane_addr, pc, a.work + jn, a.g_pos + jn, nn, q, (warp - kTmWorkers) >> 2,
+                        (32 - kTmWorkers) / 4);
+        } else {
+            const bool go = ok && grp_bad == 0 && csr_ok;
+            if (go) {
+                for (int m = 2; m <= MM; ++m)
+                    group_sums(vals, grp[m - 1], m, grpRows[m], threadIdx.x, kW);
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kW) : "memory");  // workers: sums done
+            if (go) {
+#pragma unroll
+                for (int k = 0; k < kRP; ++k) {
+                    const int32_t row = threadIdx.x + k * kW;
+                    if (row < nrows) {
+                        double v = 0.0;
+                        if (rp[k] != 0xFFFF) {
+                            if (rp[k] < ne)
+                                v = plus_zero(vals[rp[k]]);
+                            else
+                                bad = true;
+                        }
+                        qG[r0 + row] = v;
+                    }
+                }
+                for (int32_t k0 = kRP * kW + threadIdx.x; k0 < nrows; k0 += kU * kW) {
+                    uint16_t p[kU];
+#pragma unroll
+                    for (int k = 0; k < kU; ++k)
+                        p[k] = k0 + k * kW < nrows ? ld_u16(a.g_rowPos + r0 + k0 + k * kW) : 0;
+#pragma unroll
+                    for (int k = 0; k < kU; ++k)
+                        if (k0 + k * kW < nrows) {
+                            double v = 0.0;
+                            if (p[k] != 0xFFFF) {
+                                if (p[k] < ne)
+                                    v = plus_zero(vals[p[k]]);
+                                else
+                                    bad = true;
+                            }
+                            qG[r0 + k0 + k * kW] = v;
+                        }
+                }
+            }
+            if (!go && threadIdx.x == 0)
+                bad = true;
+        }
+        if (bad)
+            flag(a.err);
+        tm_sync();  // the next bucket is in TMEM; vals, grp are free
+    }
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s_taddr),
+                     "n"(kTmCols)
+                     : "memory");
 }
 
 // ------------------------------------------- fused Z^T diag(d) Z (pass 2 + 1)
@@ -1280,6 +1581,39 @@ int scatter_cs(bs_ctx *ctx, const PlanArgs &a, const bs_plan_dev *p, const doubl
                   smem_s2(p), s, a, qL);
 }
 
+// TMEM column where the staged positions start (values take 16 columns per
+// group of 1024 entries, positions 4), or -1 if a bucket does not fit.
+int tm_pos_col(const bs_plan_dev *p)
+{
+    const int64_t ng = (p->g_bucket_entries_max + kTmGroupEntries - 1) / kTmGroupEntries;
+    return 20 * ng <= kTmCols ? static_cast<int>(16 * ng) : -1;
+}
+
+// Gather pass 2: the TMEM-buffered persistent kernel (cluster 1, a bucket
+// that fits TMEM, the context's setting), else one block per bucket.
+template <int CS>
+int gather_pass2(bs_ctx *ctx, const PlanArgs &a, const bs_plan_dev *p, double *qG, cudaStream_t s)
+{
+    const int pc = tm_pos_col(p);
+    if (CS == 1 && ctx->tune.tmem && pc >= 0) {
+        // 20 summing/writing warps and 12 loading ones: measured fastest of
+        // 16/16 (the loads hide, the sums and writes slow), 20/12, 24/8 (the
+        // loads outlast the sums and writes)
+        void (*k)(PlanArgs, double *, int) = gather_bucket_tm_kernel<kTmWorkersDefault>;
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem_g2(p)));
+        if (e != cudaSuccess)
+            return bs_set_error(ctx, BS_ECUDA, "gather_bucket_tm_kernel: cudaFuncSetAttribute: %s",
+                                cudaGetErrorString(e));
+        const int grid = p->g_nbuckets < ctx->sms ? p->g_nbuckets : ctx->sms;
+        k<<<grid, kT, static_cast<size_t>(smem_g2(p)), s>>>(a, qG, pc);
+        BS_LAUNCH_CHECK(ctx, "gather_bucket_tm_kernel");
+        return BS_OK;
+    }
+    return launch(ctx, "gather_bucket_kernel", gather_bucket_kernel<CS>, CS, p->g_nbuckets,
+                  smem_g2(p), s, a, qG);
+}
+
 template <int CS>
 int gather_cs(bs_ctx *ctx, const PlanArgs &a, const bs_plan_dev *p, const double *qL, double *qG,
               cudaStream_t s)
@@ -1287,8 +1621,7 @@ int gather_cs(bs_ctx *ctx, const PlanArgs &a, const bs_plan_dev *p, const double
     if (int st = launch(ctx, "gather_tile_kernel", gather_tile_kernel<CS>, CS, p->g_ntiles,
                         smem_g1(p), s, a, qL))
         return st;
-    return launch(ctx, "gather_bucket_kernel", gather_bucket_kernel<CS>, CS, p->g_nbuckets,
-                  smem_g2(p), s, a, qG);
+    return gather_pass2<CS>(ctx, a, p, qG, s);
 }
 
 } // namespace
@@ -1345,6 +1678,5 @@ int bs_apply_diag_planned(bs_ctx *ctx, const bs_gs_dev *t, const double *xG, con
                         a, static_cast<const double *>(ws), dL, wg))
         return st;
     a.work = wg;
-    return launch(ctx, "gather_bucket_kernel", gather_bucket_kernel<1>, 1, p->g_nbuckets,
-                  smem_g2(p), s, a, yG);
+    return gather_pass2<1>(ctx, a, p, yG, s);
 }

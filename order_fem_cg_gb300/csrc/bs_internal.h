@@ -24,6 +24,8 @@ struct bs_tune {
                                // tiles/buckets, 0 one block per tile/bucket
     int l2_prefetch;           // persistent two-pass kernels: 1 prefetch each block's next
                                // tile/bucket into L2 while it works on the current one
+    int tmem;                  // gather pass 2 stages the next bucket in TMEM (1, default:
+                               // measured faster) or holds one bucket at a time (0)
     int small_onepass;         // 1: one-pass gather/scatter for L2-sized vectors even with a
                                // plan (bs_gather / bs_scatter); 0: always the plan
 };

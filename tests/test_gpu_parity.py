@@ -546,6 +546,32 @@ def test_apply_diag(cfg, sizes):
     assert bs.default_context().device_status() == bs.BS_OK
 
 
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_gather_pass2_without_tmem_buffer(name, monkeypatch):
+    """Gather pass 2 has two kernels: by default the persistent one that
+    stages the next bucket in tensor memory, and the one-bucket-per-block
+    kernel (BS_TUNE_TMEM=0 at context creation).  Both are bit-exact to the
+    oracle; this keeps the second one covered."""
+    cfg = gen.WORKLOADS[name]
+    m, t, ids = mesh_case(cfg, planned=True)
+    monkeypatch.setenv("BS_TUNE_TMEM", "0")
+    ctx = bs.Context()
+    monkeypatch.delenv("BS_TUNE_TMEM")
+    qL = gen.uniform_pm1(cfg.seed, gen.TAG_U, cfg.NL)
+    ref = oracle.gather(ids, qL, cfg.NG)
+    for c in (ctx, None):
+        out = dev(np.full(cfg.NG, np.nan))
+        bs.bs_gather(t, dev(qL), out, ctx=c)
+        assert bits_equal(host(out), ref)
+    x = gen.uniform_pm1(cfg.seed, gen.TAG_X, cfg.NG)
+    d = gen.mass_diagonal(cfg.E, cfg.N)
+    yd = dev(np.full(cfg.NG, np.nan))
+    bs.bs_apply_diag(t, dev(x), dev(d), yd, ctx=ctx)
+    assert bits_equal(host(yd), oracle.apply_diag(ids, d, x))
+    assert ctx.device_status() == bs.BS_OK
+    ctx.close()
+
+
 def test_apply_diag_rejects_unfusable_plans():
     cfg = gen.WORKLOADS["tiny"]
     x, d = dev(np.ones(cfg.NG)), dev(np.ones(cfg.NL))
