@@ -60,10 +60,10 @@ KERNEL_SRC = {
 STEP_KERNELS = [
     ("copy_kernel", "copy"), ("axpy_kernel", "axpy"), ("dot_kernel", "norm"),
     ("dot_kernel", "dot"), ("cg_kernel", "cg_update"), ("gather_tile_kernel", "gather"),
-    ("gather_bucket_kernel", "gather"), ("scatter_tile_kernel", "scatter"),
+    ("gather_bucket_tm_kernel", "gather"), ("scatter_tile_kernel", "scatter"),
     ("scatter_bucket_kernel", "scatter"), ("scatter_tile_kernel", "cg_iteration"),
     ("scatter_bucket_kernel", "cg_iteration"), ("gather_tile_kernel", "cg_iteration"),
-    ("gather_bucket_kernel", "cg_iteration"), ("dot_kernel", "cg_iteration"),
+    ("gather_bucket_tm_kernel", "cg_iteration"), ("dot_kernel", "cg_iteration"),
     ("cg_kernel", "cg_iteration"), ("dot_kernel", "cg_iteration"),
 ]
 
@@ -93,10 +93,14 @@ def parse_args(argv=None):
     ap.add_argument("--cg-iters", type=int, default=20)
     ap.add_argument("--no-plan", action="store_true",
                     help="one-pass gather/scatter kernels instead of the two-pass plan")
-    ap.add_argument("--traffic-from", metavar="CSV",
-                    help="write profiles/ncu_traffic.json from an ncu launch list (CSV with "
-                         "gpu__time_duration.sum, dram__bytes_read.sum, dram__bytes_write.sum) "
-                         "of a default two-pass step, then exit")
+    ap.add_argument("--cg-no-compare", action="store_true",
+                    help="--cg-solve on --config only (skip the tiny- and mid-mesh comparisons)")
+    ap.add_argument("--traffic-from", metavar="CSV", nargs="+",
+                    help="write profiles/ncu_traffic.json from per-kernel ncu captures (CSV with "
+                         "dram__bytes_read.sum, dram__bytes_write.sum, gpu__time_duration.sum) "
+                         "of one default step on --traffic-capture, scaled to --config, then exit")
+    ap.add_argument("--traffic-capture", default="large", choices=sorted(gen.WORKLOADS),
+                    help="the mesh the --traffic-from captures ran on")
     ap.add_argument("--soak", type=float, default=1.5,
                     help="seconds of untimed steps before warm-up (clock sampling)")
     return ap.parse_args(argv)
@@ -885,6 +889,14 @@ def run_cg_solve(args):
     # per iteration: y = A p (x, y, d, one index per local), p.Ap, BS5, p update
     nbytes = 16 * cfg.NG + 12 * cfg.NL + 16 * cfg.NG + 48 * cfg.NG + 24 * cfg.NG
     peak, src = measured_peak()
+    if args.cg_no_compare:
+        print(json.dumps({
+            "mode": "cg_solve", "workload": cfg.name, "operator": "A = Z^T diag(GLL mass) Z",
+            "iters": K, "rr_ratio": rr_ratio, "eager_ms_per_iter": eager,
+            "graph_ms_per_iter": graph, "bytes_per_iter": nbytes,
+            "GB/s": nbytes / (graph * 1e-3) / 1e9, "frac": nbytes / (graph * 1e-3) / 1e9 / peak,
+            "peak_source": src}), flush=True)
+        return 0
     tiny = gen.WORKLOADS["tiny"]
     t_eager, t_graph, _ = cg_solve_times(tiny, 50, 20, 3, torch, bs, dev)
     t_fused = cg_fused_times(tiny, 50, 20, 3, torch, bs, dev)
@@ -907,8 +919,8 @@ def run_cg_solve(args):
     return 0
 
 
-def traffic_from_csv(path, config):
-    """Per-operation DRAM bytes per call from an ncu launch list of bench steps."""
+def _ncu_launches(path):
+    """{kernel: [(ID, dram bytes, ns), ...] in launch order} of an ncu --csv log."""
     import csv
     import io
     import re
@@ -921,24 +933,53 @@ def traffic_from_csv(path, config):
             continue
         rec = launches.setdefault(int(r["ID"]), {"kernel": m.group(1)})
         rec[r["Metric Name"]] = float(r["Metric Value"].replace(",", ""))
-    seq = [launches[i] for i in sorted(launches)]
-    steps = [seq[i:i + len(STEP_KERNELS)] for i in range(0, len(seq), len(STEP_KERNELS))]
-    steps = [st for st in steps if len(st) == len(STEP_KERNELS) and
-             all(k["kernel"] == want for k, (want, _) in zip(st, STEP_KERNELS))]
-    if not steps:
-        raise SystemExit("no complete default step found in the launch list")
+    out = {}
+    for i in sorted(launches):
+        k = launches[i]
+        out.setdefault(k["kernel"], []).append(
+            (i, k.get("dram__bytes_read.sum", 0.0) + k.get("dram__bytes_write.sum", 0.0),
+             k.get("gpu__time_duration.sum", 0.0)))
+    return out
+
+
+def traffic_from_csv(paths, capture, target):
+    """Per-operation DRAM bytes per call from per-kernel ncu captures of one
+    bench step on the `capture` mesh (each log one kernel family, its first
+    launches in step order), scaled to the `target` mesh by the operation's
+    moved-bytes model (perfmodel.moved_bytes)."""
+    per_kernel = {}
+    for p in paths:
+        for k, v in _ncu_launches(p).items():
+            per_kernel.setdefault(k, []).extend(v)
+    used = {}
+    ops = {}
+    for kernel, op in STEP_KERNELS:
+        i = used.get(kernel, 0)
+        used[kernel] = i + 1
+        seq = per_kernel.get(kernel, [])
+        if i >= len(seq):
+            continue
+        rec = ops.setdefault(op, {"bytes": 0.0, "ns": 0.0, "kernels": []})
+        rec["bytes"] += seq[i][1]
+        rec["ns"] += seq[i][2]
+        rec["kernels"].append(kernel)
+    pm = bs_perf()
+    cw, tw = gen.WORKLOADS[capture], gen.WORKLOADS[target]
     out = {}
     for op in KERNEL_SRC:
-        per = []
-        for st in steps:
-            b = sum(k["dram__bytes_read.sum"] + k["dram__bytes_write.sum"]
-                    for k, (_, o) in zip(st, STEP_KERNELS) if o == op)
-            per.append(b)
-        out[op] = {"bytes_per_launch": sum(per) / len(per), "config": config,
-                   "src_sha256": src_sha(KERNEL_SRC[op]), "steps": len(per)}
-    doc = {"source": os.path.basename(path), "note": "dram__bytes_read.sum + "
-           "dram__bytes_write.sum per call of each operation (all of its kernels), averaged "
-           "over the captured steps", "kernels": out}
+        want = [k for k, o in STEP_KERNELS if o == op]
+        if op not in ops or ops[op]["kernels"] != want:
+            continue
+        scale = (pm.moved_bytes(op, tw.NL, tw.NG, tw.NL) / pm.moved_bytes(op, cw.NL, cw.NG, cw.NL))
+        out[op] = {"bytes_per_launch": ops[op]["bytes"] * scale, "config": target,
+                   "measured_bytes": ops[op]["bytes"], "measured_us": ops[op]["ns"] / 1e3,
+                   "measured_on": capture, "scale": scale, "kernels": want,
+                   "src_sha256": src_sha(KERNEL_SRC[op])}
+    doc = {"source": [os.path.basename(p) for p in paths],
+           "note": f"dram__bytes_read.sum + dram__bytes_write.sum of each operation's kernels "
+                   f"(first call in one bench step), measured on the {capture} mesh, one kernel "
+                   f"family per ncu capture, scaled to the {target} mesh by the operation's "
+                   "moved-bytes model", "kernels": out}
     with open(TRAFFIC_FILE, "w") as f:
         json.dump(doc, f, indent=1)
     print(json.dumps(doc, indent=1))
@@ -948,7 +989,7 @@ def traffic_from_csv(path, config):
 def main(argv=None):
     args = parse_args(argv)
     if args.traffic_from:
-        return traffic_from_csv(args.traffic_from, args.config)
+        return traffic_from_csv(args.traffic_from, args.traffic_capture, args.config)
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

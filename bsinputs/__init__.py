@@ -174,7 +174,10 @@ class MeshConfig:
 # The benchmark workloads: four box meshes (tiny, mid, large, stress) and the
 # vector-length sweep 2^10 .. 2^27 for the five mesh-free operations; plus
 # the stress mesh with Dirichlet-masked boundary nodes and randomly oriented
-# elements (an unstructured-like numbering) at the same scale.
+# elements (an unstructured-like numbering) at the same scale; plus "probe",
+# the stress mesh's degree on 48^3 elements: every vector beyond L2 (191 MB
+# local, 112 MB global) with a few GB on the device, the size hardware
+# counters are captured at.
 WORKLOADS = {
     "tiny": MeshConfig("tiny", 8, 3, SEED_BASE + 0),
     "mid": MeshConfig("mid", 20, 7, SEED_BASE + 1),
@@ -182,6 +185,7 @@ WORKLOADS = {
     "stress": MeshConfig("stress", 64, 5, SEED_BASE + 4),
     "stress_masked": MeshConfig("stress_masked", 64, 5, SEED_BASE + 5,
                                 SHUFFLE_ELEMS | PERMUTE_GLOBAL | MASK_BOUNDARY | ROTATE_ELEMS),
+    "probe": MeshConfig("probe", 48, 5, SEED_BASE + 6),
 }
 SWEEP_SEED = SEED_BASE + 2
 SWEEP_LOG2 = tuple(range(10, 28))

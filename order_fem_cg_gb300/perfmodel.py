@@ -79,3 +79,34 @@ def bytes_cg_iteration(NL, NG, nnz, nblocks):
     """scatter + gather + dot + fused update + norm on global-length vectors."""
     return (bytes_scatter(NL, NG) + bytes_gather(NL, NG, nnz, nblocks) + bytes_dot(NG)
             + bytes_cg_update(NG) + bytes_norm(NG))
+
+
+# ------------------------------------------------ DRAM traffic of the design
+
+def moved_bytes(op, NL, NG, nnz):
+    """Bytes the library's kernels move for one call (not the figure of
+    merit: the algorithmic bytes above are).  Streaming operations move
+    their algorithmic bytes.  The two-pass gather and scatter route every
+    local value through a work array in HBM: scatter reads q_G and its
+    pass-1 offsets, writes the work array, reads it back with its pass-2
+    offsets and writes q_L (8 N_G + 20 nnz + 8 N_L); gather reads q_L and
+    its offsets, writes and reads the work array with its offsets, reads
+    each row's staged position and writes q_G (8 NL + 20 nnz + 10 N_G).
+    Run tables (under 5%) are left out.  Used to scale DRAM traffic measured
+    on one mesh to another."""
+    n = NL
+    if op == "copy":
+        return bytes_copy(n)
+    if op == "axpy":
+        return bytes_axpy(n)
+    if op == "norm":
+        return bytes_norm(n)
+    if op == "dot":
+        return bytes_dot(n)
+    if op == "cg_update":
+        return bytes_cg_update(n)
+    if op == "scatter":
+        return 8 * NG + 20 * nnz + 8 * NL
+    if op == "gather":
+        return 8 * NL + 20 * nnz + 10 * NG
+    raise ValueError(op)
