@@ -791,10 +791,15 @@ def run_mass_operator(args):
 
     fused = timed(lambda: bs.bs_apply_diag(t, x, d, y), args.steps)
     separate = timed(lambda: (bs.bs_scatter(t, x, qL), bs.bs_gather(t, qL, y)), args.steps)
+    # the same arithmetic unfused: scatter, the elementwise product (torch's
+    # kernel, one binary64 multiply per local), gather
+    unfused = timed(lambda: (bs.bs_scatter(t, x, qL), qL.mul_(d), bs.bs_gather(t, qL, y)),
+                    args.steps)
     nbytes = 16 * cfg.NG + 12 * cfg.NL   # read x, d, ids; write y
     peak, src = measured_peak()
     print(json.dumps({"mode": "mass_operator", "workload": cfg.name, "op": "y = Z^T diag(d) Z x",
                       "fused_ms": fused, "scatter_plus_gather_ms": separate,
+                      "scatter_times_d_gather_ms": unfused,
                       "algorithmic_bytes": nbytes, "fused_GB/s": nbytes / (fused * 1e-3) / 1e9,
                       "fused_frac": nbytes / (fused * 1e-3) / 1e9 / peak, "peak_source": src,
                       "steps": args.steps}), flush=True)
