@@ -166,22 +166,24 @@ __device__ __forceinline__ void finish_reduction(double v, const RedOut &o)
 // squares with one fma per element is bound by the FP64 pipe below HBM
 // speed.  SqAcc forms x^2 and sums it on the FP32 and integer pipes:
 //   |x| = xh + xl + dx with xh the leading 24 significant bits (a float,
-//   exact), xl the next 23 bits (exact float) and dx the last 6 bits,
-//   dropped: 0 <= dx < 2^-46 |x|; built with integer and FP32 operations
-//   only (on this part int<->float conversions are as scarce as FP64 math);
-//   x^2 ~= xh^2 + (2 xh xl + xl^2), xh^2 exact as p + e (TwoProduct by
-//   fmaf); p is added to a float-float sum (s, c) by TwoSum (exact), the
-//   small terms q = e + 2 xh xl + xl^2 (two fmaf roundings) to c.  Every
-//   chunk of at most 8 elements is flushed: (s, c) move into a binary64
-//   total through an exact float->double conversion on the integer pipe.
+//   exact), xl the next 23 bits and dx the last 6 bits, dropped:
+//   0 <= dx < 2^-46 |x|; 2 xl is formed exactly as the float difference
+//   2^k (1 + f) - 2^k (Sterbenz) from integer operations only (on this
+//   part int<->float conversions are as scarce as FP64 math);
+//   x^2 ~= xh^2 + 2 xh xl, xh^2 exact as p + e (TwoProduct by fmaf), q =
+//   fma(xh, 2 xl, e) rounded once; p is added to a float-float sum (s, c)
+//   by Fast2Sum with the larger of s, p first (both are >= 0: exact), q
+//   and the addition's error to c.  Every chunk of at most 8 elements is
+//   flushed: (s, c) move into a binary64 total through an exact
+//   float->double conversion on the integer pipe.
 // Worst case, for a chunk with exact sum S of squares (all terms >= 0):
-//   dropped bits: x^2 underestimated by <= 2^-45 x^2;
-//   q's two roundings: <= 2 * 2^-24 * 1.25 * 2^-22 x^2 = 1.25 * 2^-45 x^2;
-//   c: every term t_j = err_j + q_j has |err_j| <= 2^-24 S (TwoSum's exact
-//   rounding error of s) and sum |q_j| <= 1.25 * 2^-22 S, so |c| <=
-//   (k 2^-24 + 1.25 * 2^-22) S = 3.25 * 2^-22 S for k = 8, and its k + k
-//   float roundings add <= 2^-24 (1 + k) * 3.25 * 2^-22 S = 29.25 * 2^-46 S;
-//   in all <= 2.25 * 2^-45 S + 29.25 * 2^-46 S < 4.8e-13 S, plus the binary64
+//   dropped bits dx and the left-out xl^2: x^2 underestimated by
+//   <= 2^-45 x^2 + 2^-46 x^2; q's rounding: <= 2^-24 * 1.25 * 2^-22 x^2;
+//   c: every term t_j = err_j + q_j has |err_j| <= 2^-24 S and
+//   sum |q_j| <= 1.25 * 2^-22 S, so |c| <= (k 2^-24 + 1.25 * 2^-22) S =
+//   3.25 * 2^-22 S for k = 8, and its k + k float roundings add
+//   <= 2^-24 (1 + k) * 3.25 * 2^-22 S = 29.25 * 2^-46 S;
+//   in all < 2.1 * 2^-45 S + 29.25 * 2^-46 S < 4.8e-13 S, plus the binary64
 //   flushes and the fixed reduction tree (2^-53 per addition).  So the
 //   total is within 5e-13 relative of the exact sum of squares.  |x|
 //   outside [2^-40, 2^41) (subnormal, tiny, huge, inf, NaN) goes through a
@@ -225,19 +227,17 @@ struct SqAcc {
         if (fast) {
             const uint32_t t = hw - ((1023u - 127u) << 20);
             const float xh = __uint_as_float(__funnelshift_l(lw, t, 3));
-            // xl: bits 6..28 of the fraction as an exact float (2^23 + k) - 2^23,
-            // scaled by 2^(e-46); the 6 dropped bits are below 2^-46 |x|.
-            const float k23 = __fsub_rn(
-                __uint_as_float(0x4B000000u | ((lw & 0x1FFFFFFFu) >> 6)), 8388608.0f);
-            const float scale = __uint_as_float((E - (1023u + 46u - 127u)) << 23);
-            const float xl = __fmul_rn(k23, scale);
+            // 2 xl: bits 6..28 of the fraction as the mantissa f of a float
+            // 2^k (1 + f), minus 2^k, k = e - 22 (e: x's exponent); exact
+            const uint32_t one = (E - (1023u + 22u - 127u)) << 23;
+            const float xl2 = __fsub_rn(__uint_as_float(one | ((lw & 0x1FFFFFFFu) >> 6)),
+                                        __uint_as_float(one));
             const float p = __fmul_rn(xh, xh);
-            float q = __fmaf_rn(xh, xh, -p);
-            q = __fmaf_rn(__fadd_rn(xh, xh), xl, q);
-            q = __fmaf_rn(xl, xl, q);
-            const float sn = __fadd_rn(s, p);
-            const float bp = __fsub_rn(sn, s);
-            const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(sn, bp)), __fsub_rn(p, bp));
+            float q = __fmaf_rn(xh, xh, -p);  // exact: xh^2 = p + q
+            q = __fmaf_rn(xh, xl2, q);        // + 2 xh xl
+            const float a = fmaxf(s, p), b = fminf(s, p);
+            const float sn = __fadd_rn(a, b);
+            const float err = __fsub_rn(b, __fsub_rn(sn, a));  // exact (a >= b >= 0)
             s = sn;
             c = __fadd_rn(c, __fadd_rn(err, q));
         }
