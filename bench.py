@@ -93,6 +93,9 @@ def parse_args(argv=None):
     ap.add_argument("--cg-iters", type=int, default=20)
     ap.add_argument("--no-plan", action="store_true",
                     help="one-pass gather/scatter kernels instead of the two-pass plan")
+    ap.add_argument("--norm-ab", action="store_true",
+                    help="BS3 norm at n = N_L of --config timed after a read-only operation "
+                         "and after operations that write N_L values (AXPY, copy)")
     ap.add_argument("--cg-no-compare", action="store_true",
                     help="--cg-solve on --config only (skip the tiny- and mid-mesh comparisons)")
     ap.add_argument("--traffic-from", metavar="CSV", nargs="+",
@@ -448,15 +451,32 @@ class OracleSample:
                 + pm.bytes_cg_iteration(NL, NG, NL, 0))
         self.bytes = frac * full
 
-    def step(self):
+    def step(self, times=None):
+        """One sampled step; with `times` (a dict), adds each operation's
+        wall time to it."""
         o, cfg, m, mg = self.oracle, self.cfg, self.m, self.mg
+        clock = time.perf_counter
+        t = [clock()]
+
+        def mark(name):
+            t.append(clock())
+            if times is not None:
+                times[name] = times.get(name, 0.0) + t[-1] - t[-2]
+
         o.copy(self.u)
+        mark("copy")
         o.axpy(cfg.alpha, self.p, cfg.beta, self.r)
+        mark("axpy")
         o.norm(self.Ap)
+        mark("norm")
         o.dot(self.x, self.u)
+        mark("dot")
         o.cg_update(cfg.alpha, self.p, self.Ap, self.x, self.r)
+        mark("cg_update")
         o.gather(self.ids[:m], self.u, cfg.NG)
+        mark("gather")
         o.scatter(self.ids[:m], self.qG)
+        mark("scatter")
         # CG sequence on the sample: scatter/gather over m local entries,
         # vector operations over the first mg global entries
         pL = o.scatter(self.ids[:m], self.pG)
@@ -465,6 +485,25 @@ class OracleSample:
         _, r1, _ = o.cg_update(1.0 / (pAp or 1.0), self.pG[:mg], ApG[:mg], self.xG[:mg],
                                self.rG[:mg])
         o.norm(r1)
+        mark("cg_iteration")
+
+    def per_op(self, times, reps):
+        """Per-operation oracle figures from accumulated step times: seconds
+        per full (unsampled) call and GB/s of the operation's sampled
+        algorithmic bytes."""
+        pm = bs_perf()
+        cfg, f = self.cfg, self.frac
+        NL, NG = cfg.NL, cfg.NG
+        full = {"copy": pm.bytes_copy(NL), "axpy": pm.bytes_axpy(NL), "norm": pm.bytes_norm(NL),
+                "dot": pm.bytes_dot(NL), "cg_update": pm.bytes_cg_update(NL),
+                "gather": pm.bytes_gather(NL, NG, NL, 0), "scatter": pm.bytes_scatter(NL, NG),
+                "cg_iteration": pm.bytes_cg_iteration(NL, NG, NL, 0)}
+        out = {}
+        for k, sec in times.items():
+            per_call = sec / reps
+            out[k] = {"ms_per_full_call": per_call / f * 1e3,
+                      "GB/s": f * full[k] / per_call / 1e9}
+        return out
 
     def describe(self):
         return (f"oracle (single-threaded C, Dot2 reductions) on {self.frac:.4g} of the step: "
@@ -641,16 +680,17 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         samp = OracleSample(cfg, args.cpu_sample, host=wl.h)
         reps = 0
+        op_times = {}
         t0 = time.perf_counter()
         while True:
-            samp.step()
+            samp.step(op_times)
             reps += 1
             dt = time.perf_counter() - t0
             if dt >= args.cpu_seconds or reps >= 50:
                 break
         cpu = {"value": samp.bytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": f"{reps} x " + samp.describe(), "seconds": dt,
-               "host": host_cpu()}
+               "host": host_cpu(), "per_op": samp.per_op(op_times, reps)}
 
     if rank == 0:
         line = {
@@ -759,6 +799,51 @@ def run_sweep(args):
                             "GB/s_host": p[1] / p[2] / 1e9, "GB/s_event": p[1] / p[3] / 1e9}
                            for p in pts]}
         print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_norm_ab(args):
+    """BS3 inside a sequence: the norm of its own vector timed (CUDA events
+    around it alone) right after another operation on other vectors.  A
+    preceding operation that wrote N_L values leaves up to L2's worth of
+    dirty lines, which HBM writes back while the norm reads."""
+    import torch
+
+    import order_fem_cg_gb300 as bs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cfg = gen.WORKLOADS[args.config]
+    n = cfg.NL
+
+    def vec(tag):
+        return torch.from_numpy(gen.uniform_pm1(cfg.seed, tag, n)).to(dev)
+
+    x, y, z, w = vec(1), vec(2), vec(3), vec(4)
+    out = torch.empty(1, dtype=torch.float64, device=dev)
+    s = torch.cuda.current_stream()
+    peak, src = measured_peak()
+    cases = {"after_dot": lambda: bs.bs_dot(x, y),
+             "after_norm": lambda: bs.bs_norm(w),
+             "after_axpy": lambda: bs.bs_axpy(0.37, x, 1.0, y),
+             "after_copy": lambda: bs.bs_copy(x, y)}
+    res = {}
+    for name, pre in cases.items():
+        ts = []
+        for i in range(max(3, args.warmup) + max(5, min(args.steps, 50))):
+            pre()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            bs.bs_norm(z, out)
+            e1.record(s)
+            e1.synchronize()
+            if i >= max(3, args.warmup):
+                ts.append(e0.elapsed_time(e1) * 1e3)
+        med = statistics.median(ts)
+        res[name] = {"median_us": med, "min_us": min(ts),
+                     "GB/s": 8 * n / (med * 1e-6) / 1e9, "frac": 8 * n / (med * 1e-6) / 1e9 / peak}
+    print(json.dumps({"mode": "norm_ab", "workload": cfg.name, "n": n, "peak_source": src,
+                      "cases": res}), flush=True)
     return 0
 
 
@@ -999,6 +1084,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.norm_ab:
+        return run_norm_ab(args)
     if args.mass_operator:
         return run_mass_operator(args)
     if args.cg_solve:
