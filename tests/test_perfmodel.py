@@ -42,3 +42,19 @@ def test_byte_counts_of_the_workload_meshes():
     lg = gen.WORKLOADS["large"]
     seq = pm.bytes_cg_iteration(lg.NL, lg.NG, lg.NL, 0) - 4 - 4
     assert seq == 24 * lg.NL + 92 * lg.NG
+
+
+def test_moved_bytes_of_the_two_pass_design():
+    """The two-pass gather and scatter route every entry through the work
+    array (8 bytes written, 8 read, a 16-bit offset each way); their ceiling
+    on the stress mesh is the algorithmic / moved ratio."""
+    import bsinputs as gen
+    c = gen.WORKLOADS["stress"]
+    NL, NG = c.NL, c.NG
+    assert pm.moved_bytes("gather", NL, NG, NL) == 8 * NL + 20 * NL + 10 * NG
+    assert pm.moved_bytes("scatter", NL, NG, NL) == 8 * NG + 20 * NL + 8 * NL
+    for op, n in (("copy", 16), ("axpy", 24), ("norm", 8), ("dot", 16), ("cg_update", 48)):
+        assert pm.moved_bytes(op, NL, NG, NL) == n * NL
+    g = pm.bytes_gather(NL, NG, NL, 0) / pm.moved_bytes("gather", NL, NG, NL)
+    s = pm.bytes_scatter(NL, NG) / pm.moved_bytes("scatter", NL, NG, NL)
+    assert abs(g - 0.562) < 0.001 and abs(s - 0.510) < 0.001
