@@ -110,6 +110,11 @@ __device__ __forceinline__ uint2 ld_u16x4(const uint16_t *p)
     return v;
 }
 
+__device__ __forceinline__ void st_pair(double *p, double x, double y)
+{
+    asm volatile("st.global.v2.f64 [%0], {%1, %2};" ::"l"(p), "d"(x), "d"(y) : "memory");
+}
+
 __device__ __forceinline__ void flag(int *err)
 {
     atomicOr(err, BS_DEVERR_BOUNDS);
@@ -1305,13 +1310,27 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_tm_kernel(PlanArgs a, dou
             grp_bad = bad;
         }
         bool bad = ok ? tm_place(lane_addr, pc, vals, ne, q, warp >> 2, 8) : false;
-        constexpr int kRP = 16;
-        uint16_t rp[kRP];
-        if (worker) {  // the first rows' staged positions, in flight during the sums
+        // The rows' staged positions, in flight during the sums: worker i
+        // holds rows rb + 2 (i + k kW) + {0, 1}, k < kRP (rb = r0 rounded
+        // down to even), their positions read two at a time and their
+        // values stored two at a time where both rows are in the bucket and
+        // the arrays allow; rows past 2 kRP kW of the bucket are read as they
+        // are written.
+        constexpr int kRP = 11;
+        uint32_t rp[kRP];
+        const int32_t rb = r0 & ~1;
+        const bool pairs = (reinterpret_cast<uintptr_t>(a.g_rowPos) & 3u) == 0 &&
+                           (reinterpret_cast<uintptr_t>(qG) & 15u) == 0;
+        if (worker) {
 #pragma unroll
             for (int k = 0; k < kRP; ++k) {
-                const int32_t row = threadIdx.x + k * kW;
-                rp[k] = ok && row < nrows ? ld_u16(a.g_rowPos + r0 + row) : 0;
+                const int32_t row = rb + 2 * (static_cast<int32_t>(threadIdx.x) + k * kW);
+                const bool in0 = ok && row >= r0 && row < r1, in1 = ok && row + 1 >= r0 && row + 1 < r1;
+                if (pairs && in0 && in1)
+                    rp[k] = ld_u16x2(a.g_rowPos + row);
+                else
+                    rp[k] = (in0 ? static_cast<uint32_t>(ld_u16(a.g_rowPos + row)) : 0xFFFFu) |
+                             ((in1 ? static_cast<uint32_t>(ld_u16(a.g_rowPos + row + 1)) : 0xFFFFu) << 16);
             }
         }
         tm_sync();  // placements landed, grpRows ready; TMEM is free
@@ -1329,38 +1348,36 @@ __global__ void __launch_bounds__(kT, 1) gather_bucket_tm_kernel(PlanArgs a, dou
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kW) : "memory");  // workers: sums done
             if (go) {
+                // a row's value: its sum, +0.0 for an empty row (0xFFFF)
+                auto value = [&](uint32_t p) {
+                    double v = 0.0;
+                    if (p != 0xFFFFu) {
+                        if (p < static_cast<uint32_t>(ne))
+                            v = plus_zero(vals[p]);
+                        else
+                            bad = true;
+                    }
+                    return v;
+                };
 #pragma unroll
                 for (int k = 0; k < kRP; ++k) {
-                    const int32_t row = threadIdx.x + k * kW;
-                    if (row < nrows) {
-                        double v = 0.0;
-                        if (rp[k] != 0xFFFF) {
-                            if (rp[k] < ne)
-                                v = plus_zero(vals[rp[k]]);
-                            else
-                                bad = true;
-                        }
-                        qG[r0 + row] = v;
+                    const int32_t row = rb + 2 * (static_cast<int32_t>(threadIdx.x) + k * kW);
+                    const bool in0 = row >= r0 && row < r1, in1 = row + 1 >= r0 && row + 1 < r1;
+                    const double v0 = in0 ? value(rp[k] & 0xFFFFu) : 0.0;
+                    const double v1 = in1 ? value(rp[k] >> 16) : 0.0;
+                    if (pairs && in0 && in1) {
+                        st_pair(qG + row, v0, v1);
+                    } else {
+                        if (in0)
+                            qG[row] = v0;
+                        if (in1)
+                            qG[row + 1] = v1;
                     }
                 }
-                for (int32_t k0 = kRP * kW + threadIdx.x; k0 < nrows; k0 += kU * kW) {
-                    uint16_t p[kU];
-#pragma unroll
-                    for (int k = 0; k < kU; ++k)
-                        p[k] = k0 + k * kW < nrows ? ld_u16(a.g_rowPos + r0 + k0 + k * kW) : 0;
-#pragma unroll
-                    for (int k = 0; k < kU; ++k)
-                        if (k0 + k * kW < nrows) {
-                            double v = 0.0;
-                            if (p[k] != 0xFFFF) {
-                                if (p[k] < ne)
-                                    v = plus_zero(vals[p[k]]);
-                                else
-                                    bad = true;
-                            }
-                            qG[r0 + k0 + k * kW] = v;
-                        }
-                }
+                // rows past the paired ones (a bucket of more than 2 kRP kW rows)
+                for (int32_t row = rb + 2 * kRP * kW + static_cast<int32_t>(threadIdx.x); row < r1; row += kW)
+                    if (row >= r0)
+                        qG[row] = value(ld_u16(a.g_rowPos + row));
             }
             if (!go && threadIdx.x == 0)
                 bad = true;
