@@ -659,6 +659,97 @@ __device__ __forceinline__ bool emit_runs(const int64_t *runs, const int32_t *ru
     return bad;
 }
 
+// One chunk of 32 kU slots of emit_runs_lean: lane slots c0 + 32 u + lane,
+// offsets o[u]; kTail: only slots below `we` exist (the warp's last chunk).
+// Shared-memory reads are clamped into the tile (vmax) and the run table
+// (cmax); a value out of range sets the returned flag.
+template <bool kTail>
+__device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kU], int32_t c0, int32_t we,
+                                               int32_t &before, uint32_t le_mask, const double *tile,
+                                               uint32_t vmax, const int32_t *runD, uint32_t cmax,
+                                               double *work, uint32_t nwork)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t bad = 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+        const int32_t k = c0 + 32 * u + lane;
+        const uint32_t raw = o[u];
+        const uint32_t starts = __ballot_sync(0xffffffffu, raw & kRunStart);
+        const uint32_t c = static_cast<uint32_t>(before + __popc(starts & le_mask));
+        before += __popc(starts);
+        const uint32_t off = raw & (kRunStart - 1u);
+        const double v = tile[min(off, vmax)];
+        const uint32_t d = static_cast<uint32_t>(runD[min(c, cmax)]) + static_cast<uint32_t>(k);
+        const bool in = !kTail || k < we;
+        bad |= static_cast<uint32_t>(in && (off > vmax || c > cmax || d >= nwork));
+        if (in && d < nwork)
+            work[d] = v;
+    }
+    return bad;
+}
+
+// emit_runs for one block (cluster 1) with fewer instructions per slot: a
+// warp's full chunks of 32 kU slots carry no per-slot range test, and the
+// table checks are clamps plus one flag instead of branches.  Same writes,
+// same checks.
+__device__ __forceinline__ bool emit_runs_lean(const int64_t *runs, const int32_t *runD, int nb,
+                                               int32_t kbeg, int32_t kend, const uint16_t *src,
+                                               int64_t base, const double *tile, int nvals,
+                                               double *work, int64_t nwork)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kT / 32;
+    const int64_t n = kend - kbeg;
+    const int32_t wb = kbeg + static_cast<int32_t>(n * warp / kWarps);
+    const int32_t we = kbeg + static_cast<int32_t>(n * (warp + 1) / kWarps);
+    if (wb >= we)
+        return false;
+    const int32_t nne = run_ci(runs[nb]);  // non-empty runs
+    if (nvals < 1 || nne < 1)
+        return true;
+    const uint32_t le_mask = (2u << lane) - 1u;
+    const int64_t rb = runs[find_run(runs, nb, wb)];
+    int32_t before = run_ci(rb) + (run_off(rb) < wb ? 1 : 0) - 1;
+    const uint32_t vmax = static_cast<uint32_t>(nvals - 1), cmax = static_cast<uint32_t>(nne - 1);
+    const uint32_t nw = static_cast<uint32_t>(nwork);  // nwork <= nnz < 2^31
+    const uint16_t *sp = src + base;
+    constexpr int32_t kChunk = 32 * kU;
+    const int32_t wf = wb + (we - wb) / kChunk * kChunk;  // end of the full chunks
+    uint32_t bad = 0;
+    uint16_t o[kU];
+    if (wb < wf) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            o[u] = ld_u16(sp + wb + 32 * u + lane);
+    }
+    for (int32_t c0 = wb; c0 < wf; c0 += kChunk) {
+        // the next chunk's offsets (or the tail's) load while this one is written
+        const int32_t c1 = c0 + kChunk;
+        uint16_t on[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int32_t k = c1 + 32 * u + lane;
+            on[u] = k < we ? ld_u16(sp + k) : 0;
+        }
+        bad |= emit_chunk<false>(o, c0, we, before, le_mask, tile, vmax, runD, cmax, work, nw);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            o[u] = on[u];
+    }
+    if (wf < we) {
+        if (wf == wb) {  // no full chunk: the tail's offsets are not loaded yet
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int32_t k = wb + 32 * u + lane;
+                o[u] = k < we ? ld_u16(sp + k) : 0;
+            }
+        }
+        bad |= emit_chunk<true>(o, wf, we, before, le_mask, tile, vmax, runD, cmax, work, nw);
+    }
+    return bad != 0;
+}
+
 template <int CS>
 __device__ __forceinline__ void cluster_barrier()
 {
@@ -932,8 +1023,12 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
             const int32_t total = s1 - s0;
             const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
             const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
-            if (emit_runs<CS>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per, len,
-                              a.work, a.nnz))
+            const bool bad = CS == 1
+                                 ? emit_runs_lean(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, vals, len,
+                                                  a.work, a.nnz)
+                                 : emit_runs<CS>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per,
+                                                 len, a.work, a.nnz);
+            if (bad)
                 flag(a.err);
         } else if (threadIdx.x == 0) {
             flag(a.err);
@@ -1461,9 +1556,7 @@ __global__ void __launch_bounds__(kT, 1)
         }
         __syncthreads();  // scaled tile ready
         if (ok) {
-            double *tile[1] = {vals};
-            if (emit_runs<1>(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, tile, len, len, wg,
-                             a.nnz))
+            if (emit_runs_lean(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, vals, len, wg, a.nnz))
                 bad = true;
         }
         if (bad || (!ok && threadIdx.x == 0))

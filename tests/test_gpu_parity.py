@@ -355,12 +355,14 @@ def test_out_of_range_entry_is_flagged_not_dereferenced():
     assert ctx.device_status() == bs.BS_OK   # the flag was cleared by the read
 
 
-def test_bad_plan_entry_is_flagged_not_dereferenced():
+@pytest.mark.parametrize("cluster", [1, 2])
+def test_bad_plan_entry_is_flagged_not_dereferenced(cluster):
     cfg = gen.WORKLOADS["tiny"]
     m = bs.Mesh(cfg.E, cfg.N, cfg.seed, cfg.flags)
-    assert m.plan(100, 64, 200, 150, 2) == bs.BS_OK
+    assert m.plan(100, 64, 200, 150, cluster) == bs.BS_OK
     pt, pi = m.plan_tables(), m.plan_info()
-    for key, bad in (("s_dst", 65535), ("s_src", 65535), ("g_src", 65535), ("g_pos", 65535)):
+    for key, bad in (("s_dst", 65535), ("s_src", 65535), ("g_src", 65535), ("g_pos", 65535),
+                     ("s_src", 0x7FFF), ("g_src", 0x7FFF)):
         corrupt = dict(pt)
         corrupt[key] = pt[key].copy()
         corrupt[key][17] = bad
