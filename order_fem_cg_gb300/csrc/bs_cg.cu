@@ -39,6 +39,7 @@ struct CgArgs {
     const int32_t *ids, *rowStarts, *localIds;
     const double *dL, *b;
     double *x, *r, *p, *Ap, *qL, *scal;
+    double mzero;  // -0 (for mul_rn)
     int32_t iters;
     double *part_a, *part_b;  // per-block partials of p.Ap and of r.r
     Bar bar;
@@ -142,7 +143,7 @@ __device__ void scatter_scaled(const CgArgs &a, const double *v)
             bad = true;
             continue;
         }
-        a.qL[l] = a.dL ? __dmul_rn(a.dL[l], v[g]) : v[g];
+        a.qL[l] = a.dL ? mul_rn(a.dL[l], v[g], a.mzero) : v[g];
     }
     if (bad)
         flag(a.err);
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kCT) cg_fused_kernel(CgArgs a)
         }
         // BS2: p = r + beta p
         for (int64_t i = t0; i < a.NG; i += stride)
-            a.p[i] = __fma_rn(1.0, a.r[i], __dmul_rn(beta, a.p[i]));
+            a.p[i] = __fma_rn(1.0, a.r[i], mul_rn(beta, a.p[i], a.mzero));
         rr = rr_new;
         if (!grid_sync(a.bar, a.err))
             return;
@@ -337,6 +338,7 @@ extern "C" int bs_cg_solve_fused(bs_ctx *ctx, const bs_gs_dev *t, const double *
     a.rowStarts = t->rowStarts;
     a.localIds = t->localIds;
     a.dL = dL;
+    a.mzero = -0.0;
     a.b = bG;
     a.x = xG;
     a.r = rG;

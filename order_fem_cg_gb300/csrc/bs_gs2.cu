@@ -52,6 +52,7 @@ struct PlanArgs {
     double *work;
     int *err;
     int pf_next;  // persistent grids: prefetch a block's next tile/bucket into L2
+    double mzero;  // -0 (for mul_rn)
 };
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p)
@@ -1551,7 +1552,7 @@ __global__ void __launch_bounds__(kT, 1)
 #pragma unroll
                 for (int q = 0; q < kU; ++q)
                     if (i0 + q * kT < len)
-                        vals[i0 + q * kT] = __dmul_rn(w[q], vals[i0 + q * kT]);
+                        vals[i0 + q * kT] = mul_rn(w[q], vals[i0 + q * kT], a.mzero);
             }
         }
         __syncthreads();  // scaled tile ready
@@ -1677,6 +1678,7 @@ PlanArgs make_args(const bs_ctx *ctx, const bs_gs_dev *t)
     a.work = p->work;
     a.err = ctx->dev_err;
     a.pf_next = ctx->tune.persist && ctx->tune.l2_prefetch;
+    a.mzero = -0.0;
     return a;
 }
 

@@ -61,6 +61,20 @@ int bs_set_error(bs_ctx *ctx, int status, const char *fmt, ...);
 // fault (bs_fault) makes it report BS_ECUDA instead, so nothing launches.
 int bs_check_device(bs_ctx *ctx, bool launching = true);
 
+#ifdef __CUDACC__
+// a * b as the fused multiply-add a * b + mzero with mzero = -0 passed in at
+// run time (a constant -0 lets the compiler turn it back into a multiply):
+// adding -0 changes no rounded product (a zero product keeps its sign), so
+// the result is bit for bit that of a multiplication, and on GB300 the FP64
+// pipe retires fused multiply-adds faster than multiplications.
+__device__ __forceinline__ double mul_rn(double a, double b, double mzero)
+{
+    double r;
+    asm("fma.rn.f64 %0, %1, %2, %3;" : "=d"(r) : "d"(a), "d"(b), "d"(mzero));
+    return r;
+}
+#endif
+
 #define BS_CUDA_TRY(ctx, call)                                                                   \
     do {                                                                                         \
         cudaError_t e_ = (call);                                                                 \

@@ -310,7 +310,7 @@ template <int V, int UNROLL, bool BETA1>
 __global__ void __launch_bounds__(kThreads) axpy_kernel(double alpha, const double *x, double beta,
                                                         double *y, int64_t h, int64_t nv,
                                                         int64_t t, const double *beta_num,
-                                                        const double *beta_den)
+                                                        const double *beta_den, double mzero)
 {
     if (!BETA1 && beta_num) {
         __shared__ double s_beta;
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(kThreads) axpy_kernel(double alpha, const doub
             if (b + u * stride < nv) {
 #pragma unroll
                 for (int k = 0; k < V; ++k) {
-                    const double by = BETA1 ? c[u].v[k] : __dmul_rn(beta, c[u].v[k]);
+                    const double by = BETA1 ? c[u].v[k] : mul_rn(beta, c[u].v[k], mzero);
                     c[u].v[k] = __fma_rn(alpha, a[u].v[k], by);
                 }
                 st_stream<V>(yv + (b + u * stride) * V, c[u]);
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) axpy_kernel(double alpha, const doub
     }
     if (gid < h + t) {
         const int64_t i = scalar_index(gid, h, nv, V);
-        const double by = BETA1 ? y[i] : __dmul_rn(beta, y[i]);
+        const double by = BETA1 ? y[i] : mul_rn(beta, y[i], mzero);
         y[i] = __fma_rn(alpha, x[i], by);
     }
 }
@@ -555,10 +555,10 @@ void launch_axpy(int grid, cudaStream_t s, double a, const double *x, double b, 
 {
     if (b == 1.0 && !bnum)
         axpy_kernel<V, kStreamUnroll, true><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv, pl.t,
-                                                                      nullptr, nullptr);
+                                                                      nullptr, nullptr, -0.0);
     else
         axpy_kernel<V, kStreamUnroll, false><<<grid, kThreads, 0, s>>>(a, x, b, y, pl.h, pl.nv,
-                                                                       pl.t, bnum, bden);
+                                                                       pl.t, bnum, bden, -0.0);
 }
 
 template <int V, bool DOT>
