@@ -887,6 +887,11 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
         const int32_t r1 = static_cast<int32_t>(min((t + 1) * TR, a.NG));
         const int32_t nrows = r1 - r0;
         const int32_t e0 = a.rowStarts[r0], e1 = a.rowStarts[r1];
+        if (pf_lane()) {  // the run writes' source offsets, read after the staging
+            int64_t p0 = e0, p1 = e1;
+            if (clamp_range(p0, p1, a.nnz))
+                prefetch_l2(a.s_src + p0, 2 * (p1 - p0));
+        }
         bool ok = a.s_tileRows[t] == r0 && a.s_tileRows[t + 1] == r1 && !st.broken;
         const int32_t m0 = min(r * a.s_tile_rows, nrows);
         const int32_t m1 = min((r + 1) * a.s_tile_rows, nrows);
@@ -1008,6 +1013,11 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
         const int32_t len =
             static_cast<int32_t>(rest < static_cast<int64_t>(CS) * per ? rest : CS * per);
         const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
+        if (pf_lane()) {  // the run writes' source offsets, read after the staging
+            int64_t p0 = s0, p1 = s1;
+            if (clamp_range(p0, p1, a.nnz))
+                prefetch_l2(a.g_src + p0, 2 * (p1 - p0));
+        }
         bool ok = len > 0 && s0 >= 0 && s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len && !st.broken;
         const int32_t m0 = ok ? min(r * per, len) : 0, m1 = ok ? min((r + 1) * per, len) : 0;
         const bool bulk = stage_start(vals, qL + l0 + m0, m1 - m0, &bar, !st.broken);
