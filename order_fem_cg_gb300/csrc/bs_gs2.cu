@@ -53,6 +53,7 @@ struct PlanArgs {
     int *err;
     int pf_next;  // persistent grids: prefetch a block's next tile/bucket into L2
     double mzero;  // -0 (for mul_rn)
+    int pf_s2;     // scatter pass 2 prefetches its bucket's later entries into L2
 };
 
 __device__ __forceinline__ uint16_t ld_u16(const uint16_t *p)
@@ -944,6 +945,13 @@ __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, doubl
         const int32_t mine = max(0, min(per, len - r * per));
         const int32_t j0 = a.s_runStart[b];
         const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + b];
+        if (a.pf_s2 && pf_lane()) {
+            int64_t p0 = j0 + 2048, p1 = j1;  // past what the first loads take
+            if (clamp_range(p0, p1, a.nnz)) {
+                prefetch_l2(a.work + p0, 8 * (p1 - p0));
+                prefetch_l2(a.s_dst + p0, 2 * (p1 - p0));
+            }
+        }
         const bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len;
         // pre-zeroed for masked locals; a bucket with as many entries as
         // locals has none (every local has exactly one entry), and every
@@ -1689,6 +1697,9 @@ PlanArgs make_args(const bs_ctx *ctx, const bs_gs_dev *t)
     a.err = ctx->dev_err;
     a.pf_next = ctx->tune.persist && ctx->tune.l2_prefetch;
     a.mzero = -0.0;
+    // only where the work array is well beyond L2: measured -7 us per stress
+    // scatter (453 MB of work entries), +1.5 us on a 134 MB one
+    a.pf_s2 = 8 * t->nnz > 2ll * ctx->l2_bytes;
     return a;
 }
 
