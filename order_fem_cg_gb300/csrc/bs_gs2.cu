@@ -628,6 +628,8 @@ __device__ __forceinline__ bool emit_runs(const int64_t *runs, const int32_t *ru
         // `we` carry offset 0 (no run start) and store nothing
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
+            if (c0 + 32 * u >= we)  // (warp-uniform) the rest of the last chunk is past the range
+                break;
             const int32_t k = c0 + 32 * u + lane;
             const uint32_t raw = o[u];
             const uint32_t starts = __ballot_sync(0xffffffffu, raw & kRunStart);
@@ -675,6 +677,8 @@ __device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kU], int32_t 
     uint32_t bad = 0;
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
+        if (kTail && c0 + 32 * u >= we)  // (warp-uniform) past the warp's range
+            break;
         const int32_t k = c0 + 32 * u + lane;
         const uint32_t raw = o[u];
         const uint32_t starts = __ballot_sync(0xffffffffu, raw & kRunStart);
@@ -911,8 +915,12 @@ __global__ void __launch_bounds__(kT, 1) scatter_tile_kernel(PlanArgs a, const d
             const int32_t total = e1 - e0;
             const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
             const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
-            if (emit_runs<CS>(runs, runD, a.s_nbuckets, kb, ke, a.s_src, e0, tile, a.s_tile_rows,
-                              nrows, a.work, a.nnz))
+            const bool bad = CS == 1
+                                 ? emit_runs_lean(runs, runD, a.s_nbuckets, kb, ke, a.s_src, e0, vals, nrows,
+                                                  a.work, a.nnz)
+                                 : emit_runs<CS>(runs, runD, a.s_nbuckets, kb, ke, a.s_src, e0, tile,
+                                                 a.s_tile_rows, nrows, a.work, a.nnz);
+            if (bad)
                 flag(a.err);
         } else if (threadIdx.x == 0) {
             flag(a.err);
