@@ -663,12 +663,18 @@ __device__ __forceinline__ bool emit_runs(const int64_t *runs, const int32_t *ru
     return bad;
 }
 
+// Steps of 32 slots per chunk of the gather runs' writes (gather pass 1 and
+// the fused operator): measured best of 2, 3, 4, 6, 8, 12, 16 on the stress
+// and large meshes (the scatter's pass 1 keeps kU: 4 was 3 us slower per
+// stress scatter).
+constexpr int kGatherEmitSteps = 4;
+
 // One chunk of 32 kU slots of emit_runs_lean: lane slots c0 + 32 u + lane,
 // offsets o[u]; kTail: only slots below `we` exist (the warp's last chunk).
 // Shared-memory reads are clamped into the tile (vmax) and the run table
 // (cmax); a value out of range sets the returned flag.
-template <bool kTail>
-__device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kU], int32_t c0, int32_t we,
+template <bool kTail, int kE>
+__device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kE], int32_t c0, int32_t we,
                                                int32_t &before, uint32_t le_mask, const double *tile,
                                                uint32_t vmax, const int32_t *runD, uint32_t cmax,
                                                double *work, uint32_t nwork)
@@ -676,7 +682,7 @@ __device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kU], int32_t 
     const int lane = threadIdx.x & 31;
     uint32_t bad = 0;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) {
+    for (int u = 0; u < kE; ++u) {
         if (kTail && c0 + 32 * u >= we)  // (warp-uniform) past the warp's range
             break;
         const int32_t k = c0 + 32 * u + lane;
@@ -699,6 +705,7 @@ __device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kU], int32_t 
 // warp's full chunks of 32 kU slots carry no per-slot range test, and the
 // table checks are clamps plus one flag instead of branches.  Same writes,
 // same checks.
+template <int kE = kU>
 __device__ __forceinline__ bool emit_runs_lean(const int64_t *runs, const int32_t *runD, int nb,
                                                int32_t kbeg, int32_t kend, const uint16_t *src,
                                                int64_t base, const double *tile, int nvals,
@@ -720,38 +727,38 @@ __device__ __forceinline__ bool emit_runs_lean(const int64_t *runs, const int32_
     const uint32_t vmax = static_cast<uint32_t>(nvals - 1), cmax = static_cast<uint32_t>(nne - 1);
     const uint32_t nw = static_cast<uint32_t>(nwork);  // nwork <= nnz < 2^31
     const uint16_t *sp = src + base;
-    constexpr int32_t kChunk = 32 * kU;
+    constexpr int32_t kChunk = 32 * kE;
     const int32_t wf = wb + (we - wb) / kChunk * kChunk;  // end of the full chunks
     uint32_t bad = 0;
-    uint16_t o[kU];
+    uint16_t o[kE];
     if (wb < wf) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u)
+        for (int u = 0; u < kE; ++u)
             o[u] = ld_u16(sp + wb + 32 * u + lane);
     }
     for (int32_t c0 = wb; c0 < wf; c0 += kChunk) {
         // the next chunk's offsets (or the tail's) load while this one is written
         const int32_t c1 = c0 + kChunk;
-        uint16_t on[kU];
+        uint16_t on[kE];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
+        for (int u = 0; u < kE; ++u) {
             const int32_t k = c1 + 32 * u + lane;
             on[u] = k < we ? ld_u16(sp + k) : 0;
         }
-        bad |= emit_chunk<false>(o, c0, we, before, le_mask, tile, vmax, runD, cmax, work, nw);
+        bad |= emit_chunk<false, kE>(o, c0, we, before, le_mask, tile, vmax, runD, cmax, work, nw);
 #pragma unroll
-        for (int u = 0; u < kU; ++u)
+        for (int u = 0; u < kE; ++u)
             o[u] = on[u];
     }
     if (wf < we) {
         if (wf == wb) {  // no full chunk: the tail's offsets are not loaded yet
 #pragma unroll
-            for (int u = 0; u < kU; ++u) {
+            for (int u = 0; u < kE; ++u) {
                 const int32_t k = wb + 32 * u + lane;
                 o[u] = k < we ? ld_u16(sp + k) : 0;
             }
         }
-        bad |= emit_chunk<true>(o, wf, we, before, le_mask, tile, vmax, runD, cmax, work, nw);
+        bad |= emit_chunk<true, kE>(o, wf, we, before, le_mask, tile, vmax, runD, cmax, work, nw);
     }
     return bad != 0;
 }
@@ -1006,7 +1013,7 @@ __global__ void __launch_bounds__(kT, 1) scatter_bucket_kernel(PlanArgs a, doubl
 // ---------------------------------------------------------------- gather
 // One cluster per tile of CS * g_tile_len locals; a grid with fewer
 // clusters than tiles loops over tiles (persistent).
-template <int CS>
+template <int CS, int kE = kGatherEmitSteps>
 __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const double *__restrict__ qL)
 {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1051,7 +1058,7 @@ __global__ void __launch_bounds__(kT, 1) gather_tile_kernel(PlanArgs a, const do
             const int32_t kb = static_cast<int32_t>(static_cast<int64_t>(total) * r / CS);
             const int32_t ke = static_cast<int32_t>(static_cast<int64_t>(total) * (r + 1) / CS);
             const bool bad = CS == 1
-                                 ? emit_runs_lean(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, vals, len,
+                                 ? emit_runs_lean<kE>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, vals, len,
                                                   a.work, a.nnz)
                                  : emit_runs<CS>(runs, runD, a.g_nbuckets, kb, ke, a.g_src, s0, tile, per,
                                                  len, a.work, a.nnz);
@@ -1583,7 +1590,8 @@ __global__ void __launch_bounds__(kT, 1)
         }
         __syncthreads();  // scaled tile ready
         if (ok) {
-            if (emit_runs_lean(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, vals, len, wg, a.nnz))
+            if (emit_runs_lean<kGatherEmitSteps>(runs, runD, a.g_nbuckets, 0, s1 - s0, a.g_src, s0, vals, len,
+                                                 wg, a.nnz))
                 bad = true;
         }
         if (bad || (!ok && threadIdx.x == 0))
