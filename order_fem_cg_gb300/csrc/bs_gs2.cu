@@ -669,7 +669,7 @@ __device__ __forceinline__ bool emit_runs(const int64_t *runs, const int32_t *ru
 // stress scatter).
 constexpr int kGatherEmitSteps = 4;
 
-// One chunk of 32 kU slots of emit_runs_lean: lane slots c0 + 32 u + lane,
+// One chunk of 32 kE slots of emit_runs_lean: lane slots c0 + 32 u + lane,
 // offsets o[u]; kTail: only slots below `we` exist (the warp's last chunk).
 // Shared-memory reads are clamped into the tile (vmax) and the run table
 // (cmax); a value out of range sets the returned flag.
@@ -702,7 +702,7 @@ __device__ __forceinline__ uint32_t emit_chunk(const uint16_t (&o)[kE], int32_t 
 }
 
 // emit_runs for one block (cluster 1) with fewer instructions per slot: a
-// warp's full chunks of 32 kU slots carry no per-slot range test, and the
+// warp's full chunks of 32 kE slots carry no per-slot range test, and the
 // table checks are clamps plus one flag instead of branches.  Same writes,
 // same checks.
 template <int kE = kU>
