@@ -548,6 +548,61 @@ def test_apply_diag(cfg, sizes):
     assert bs.default_context().device_status() == bs.BS_OK
 
 
+def adversarial_local_values(m, seed):
+    """q_L values whose row sums exercise every corner of a binary64 addition:
+    exponents over the whole range (subnormals included), signed zeros,
+    values near the largest double (sums that overflow to infinity), a few
+    +inf, rows whose entries cancel exactly or in all but their last bits, and
+    rows that add half an ulp to an even or an odd significand (rounding
+    ties)."""
+    rng = np.random.default_rng(seed)
+    NL = m.info.NL
+    sign = np.where(rng.random(NL) < 0.5, -1.0, 1.0)
+    mant = 1.0 + rng.random(NL)
+    x = sign * np.ldexp(mant, rng.integers(-40, 41, NL))
+    kind = rng.integers(0, 16, NL)
+    x[kind == 0] = (sign * np.ldexp(mant, rng.integers(-1080, 1024, NL)))[kind == 0]
+    x[kind == 1] = (sign * 0.0)[kind == 1]
+    x[kind == 2] = np.ldexp(mant, 1023)[kind == 2]  # positive: sums overflow to +inf only (no inf - inf)
+    x[(kind == 3) & (rng.random(NL) < 0.01)] = np.inf
+    tabs = m.tables()
+    rs, li = tabs["rowStarts"].astype(np.int64), tabs["localIds"].astype(np.int64)
+    rows = np.nonzero(np.diff(rs) >= 2)[0]
+    pick = rng.permutation(rows)
+    n4 = len(pick) // 4
+    a, b = li[rs[pick]], li[rs[pick] + 1]
+    base = x[a]
+    finite = np.isfinite(base) & (base != 0.0) & (np.abs(base) < 2.0 ** 1000)
+    # exact cancellation, then cancellation in all but the last bits
+    x[b[:n4]] = np.where(finite[:n4], -base[:n4], x[b[:n4]])
+    flip = np.frombuffer(np.ascontiguousarray(base[n4:2 * n4]).tobytes(), dtype=np.uint64) ^ \
+        rng.integers(1, 1 << 20, n4, dtype=np.uint64)
+    near = -np.frombuffer(flip.tobytes(), dtype=np.float64)
+    x[b[n4:2 * n4]] = np.where(finite[n4:2 * n4], near, x[b[n4:2 * n4]])
+    # ties: 2^k (even significand) or 2^k (1 + 2^-52) (odd) plus 2^(k-53)
+    k = rng.integers(-500, 500, len(pick) - 2 * n4)
+    odd = rng.random(len(k)) < 0.5
+    x[a[2 * n4:]] = np.ldexp(np.where(odd, 1.0 + 2.0 ** -52, 1.0), k)
+    x[b[2 * n4:]] = np.ldexp(1.0, k - 53) * np.where(rng.random(len(k)) < 0.5, -1.0, 1.0)
+    return x
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid"])
+def test_gather_adversarial_values(name):
+    """Row sums of adversarial values (see adversarial_local_values) through
+    the two-pass gather and the one-pass gather, bit for bit against the
+    oracle's ascending binary64 sums."""
+    cfg = gen.WORKLOADS[name]
+    for planned in (True, False):
+        m, t, ids = mesh_case(cfg, planned=planned)
+        for seed in (1, 2):
+            qL = adversarial_local_values(m, seed + 10 * cfg.seed)
+            out = dev(np.full(cfg.NG, np.nan))
+            bs.bs_gather(t, dev(qL), out)
+            assert bits_equal(host(out), oracle.gather(ids, qL, cfg.NG))
+    assert bs.default_context().device_status() == bs.BS_OK
+
+
 @pytest.mark.parametrize("name", ["tiny", "mid"])
 def test_gather_pass2_without_tmem_buffer(name, monkeypatch):
     """Gather pass 2 has two kernels: by default the persistent one that
