@@ -1556,6 +1556,13 @@ __global__ void __launch_bounds__(kT, 1)
         const int32_t len = static_cast<int32_t>(a.NL - l0 < a.g_tile_len ? a.NL - l0 : a.g_tile_len);
         const int32_t j0 = a.s_runStart[u];
         const int32_t j1 = a.s_runStart[static_cast<int64_t>(a.s_ntiles) * a.s_nbuckets + u];
+        if (a.pf_s2 && pf_lane()) {  // as in the scatter's pass 2: the range's later entries into L2
+            int64_t p0 = j0 + 2048, p1 = j1;
+            if (clamp_range(p0, p1, a.nnz)) {
+                prefetch_l2(ws + p0, 8 * (p1 - p0));
+                prefetch_l2(a.s_dst + p0, 2 * (p1 - p0));
+            }
+        }
         const int32_t s0 = a.g_tileSlot[u], s1 = a.g_tileSlot[u + 1];
         bool ok = len > 0 && j0 >= 0 && j1 >= j0 && j1 <= a.nnz && j1 - j0 <= len && s0 >= 0 &&
                   s1 >= s0 && s1 <= a.nnz && s1 - s0 <= len;
