@@ -78,6 +78,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-sample", type=float, default=1.0,
                     help="fraction of the step the oracle runs for cpu_baseline")
+    ap.add_argument("--no-all-cores", action="store_true",
+                    help="skip the all-core (OpenMP) oracle leg of cpu_baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="repeat the oracle sample until this much CPU time has passed")
     ap.add_argument("--ref-sample", type=float, default=1.0 / 32,
@@ -512,6 +514,45 @@ class OracleSample:
                 f"{self.cfg.NG} global entries; GB/s = sampled algorithmic bytes / wall time")
 
 
+def all_cores_baseline(cfg, seconds, ids=None):
+    """The oracle's loops on every host core (oracle/oracle_omp.c, OpenMP:
+    elementwise operations, scatter and gather bitwise the single-thread
+    oracle's; norm and dot by Dot2 per thread chunk, chunks combined in
+    order), run in a process of its own -- no PyTorch, so only one OpenMP
+    runtime -- over the full step for `seconds`.  A run that fails is
+    reported, not raised."""
+    import tempfile
+    cmd = [sys.executable, "-m", "oracle.allcores", cfg.name, str(seconds)]
+    with tempfile.TemporaryDirectory() as tmp:
+        if ids is not None:  # the table the single-thread leg built (saves rebuilding it)
+            path = os.path.join(tmp, "ids.npy")
+            np.save(path, np.ascontiguousarray(ids, dtype=np.int32))
+            cmd.append(path)
+        try:
+            res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True,
+                                 timeout=6 * seconds + 300)
+        except subprocess.TimeoutExpired:
+            return {"unavailable": "the all-core oracle run did not finish in time"}
+    lines = res.stdout.strip().splitlines()
+    if res.returncode != 0 or not lines:
+        why = (res.stderr.strip().splitlines() or ["no output"])[-1]
+        return {"unavailable": f"the all-core oracle run failed: {why[:200]}"}
+    d = json.loads(lines[-1])
+    pm = bs_perf()
+    NL, NG = cfg.NL, cfg.NG
+    full = {"copy": pm.bytes_copy(NL), "axpy": pm.bytes_axpy(NL), "norm": pm.bytes_norm(NL),
+            "dot": pm.bytes_dot(NL), "cg_update": pm.bytes_cg_update(NL),
+            "gather": pm.bytes_gather(NL, NG, NL, 0), "scatter": pm.bytes_scatter(NL, NG),
+            "cg_iteration": pm.bytes_cg_iteration(NL, NG, NL, 0)}
+    step_bytes = sum(full.values())
+    return {"value": step_bytes / d["s_per_step"] / 1e9, "unit": "GB/s", "cores": d["threads"],
+            "kind": "oracle loops on all host cores (OpenMP)",
+            "reductions": "Dot2 over each thread's contiguous chunk, chunks combined in order",
+            "sample": f"{d['reps']} x the full step", "seconds": d["seconds"],
+            "per_op": {k: {"ms_per_full_call": v * 1e3, "GB/s": full[k] / v / 1e9}
+                       for k, v in d["s_per_op"].items()}}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -691,6 +732,8 @@ def run_gpu(args):
         cpu = {"value": samp.bytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1,
                "kind": "oracle", "sample": f"{reps} x " + samp.describe(), "seconds": dt,
                "host": host_cpu(), "per_op": samp.per_op(op_times, reps)}
+        if not args.no_all_cores:
+            cpu["all_cores"] = all_cores_baseline(cfg, args.cpu_seconds, samp.ids)
 
     if rank == 0:
         line = {

@@ -76,6 +76,53 @@ def _load():
     return _lib
 
 
+_OMP_SRC = os.path.join(_HERE, "oracle_omp.c")
+_OMP_LIB = os.path.join(_HERE, "liboracle_omp.so")
+_omp = None
+
+
+def build_omp(force: bool = False):
+    """Compile oracle_omp.c (the oracle's loops on every core, OpenMP) into
+    liboracle_omp.so; returns its path, or None when the C compiler has no
+    OpenMP."""
+    if force or not os.path.exists(_OMP_LIB) or os.path.getmtime(_OMP_LIB) < os.path.getmtime(_OMP_SRC):
+        tmp = _OMP_LIB + f".tmp{os.getpid()}"
+        res = subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+             "-shared", "-o", tmp, _OMP_SRC, "-lm"],
+            capture_output=True,
+        )
+        if res.returncode != 0:
+            return None
+        os.replace(tmp, _OMP_LIB)
+    return _OMP_LIB
+
+
+def _load_omp():
+    global _omp
+    if _omp is None:
+        path = build_omp()
+        if path is None:
+            raise RuntimeError("no OpenMP C compiler: the all-core oracle is not available")
+        lib = ctypes.CDLL(path)
+        lib.oracle_omp_threads.restype = ctypes.c_int
+        lib.oracle_omp_copy.argtypes = [_i64, _f64p, _f64p]
+        lib.oracle_omp_axpy.argtypes = [_i64, _dbl, _f64p, _dbl, _f64p]
+        lib.oracle_omp_dot2.argtypes = [_i64, _f64p, _f64p]
+        lib.oracle_omp_dot2.restype = _dbl
+        lib.oracle_omp_cg_update.argtypes = [_i64, _dbl, _f64p, _f64p, _f64p, _f64p]
+        lib.oracle_omp_scatter.argtypes = [_i64, _i32p, _f64p, _f64p]
+        _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+        lib.oracle_omp_gather.argtypes = [_i64, _i64, _i64p, _i32p, _f64p, _f64p]
+        lib.oracle_rows.argtypes = [_i64, _i64, _i32p, _i64p, _i32p]
+        lib.oracle_rows.restype = ctypes.c_int
+        for f in (lib.oracle_omp_copy, lib.oracle_omp_axpy, lib.oracle_omp_cg_update,
+                  lib.oracle_omp_scatter, lib.oracle_omp_gather):
+            f.restype = None
+        _omp = lib
+    return _omp
+
+
 def _f64(a):
     return np.ascontiguousarray(a, dtype=np.float64)
 
@@ -238,3 +285,80 @@ def cg_solve(ids, dL, bG, xG, iters):
         rr.append(rr_new)
         p = axpy(1.0, r, _quot(rr_new, rr[k]), p)
     return dict(x=x, r=r, p=p, rr=rr, pAp=pAp)
+
+
+# ---------------------------------------------------------------------------
+# The same loops on every host core (oracle_omp.c), for the bench's all-core
+# CPU baseline.  Elementwise operations, scatter and gather are bitwise the
+# single-thread oracle's; norm and dot sum each thread's contiguous chunk by
+# Dot2 and combine the chunks in order.
+
+def omp_threads():
+    """OpenMP threads the all-core loops use."""
+    return int(_load_omp().oracle_omp_threads())
+
+
+def omp_copy(x):
+    x = _f64(x)
+    y = np.empty_like(x)
+    _load_omp().oracle_omp_copy(x.size, x, y)
+    return y
+
+
+def omp_axpy(alpha, x, beta, y):
+    x = _f64(x)
+    out = np.array(y, dtype=np.float64, copy=True, order="C")
+    assert out.size == x.size
+    _load_omp().oracle_omp_axpy(x.size, float(alpha), x, float(beta), out)
+    return out
+
+
+def omp_dot(x, y):
+    x, y = _f64(x), _f64(y)
+    assert x.size == y.size
+    return float(_load_omp().oracle_omp_dot2(x.size, x, y))
+
+
+def omp_norm(x):
+    x = _f64(x)
+    return float(_load_omp().oracle_omp_dot2(x.size, x, x))
+
+
+def omp_cg_update(alpha, p, Ap, x, r):
+    p, Ap = _f64(p), _f64(Ap)
+    xo = np.array(x, dtype=np.float64, copy=True, order="C")
+    ro = np.array(r, dtype=np.float64, copy=True, order="C")
+    n = p.size
+    assert Ap.size == n and xo.size == n and ro.size == n
+    lib = _load_omp()
+    lib.oracle_omp_cg_update(n, float(alpha), p, Ap, xo, ro)
+    return xo, ro, float(lib.oracle_omp_dot2(n, ro, ro))
+
+
+def omp_scatter(ids, qG):
+    ids, qG = _i32(ids), _f64(qG)
+    qL = np.empty(ids.size, dtype=np.float64)
+    _load_omp().oracle_omp_scatter(ids.size, ids, qG, qL)
+    return qL
+
+
+def rows_of(ids, NG):
+    """Rows of a local-to-global table (setup, not an operation): rowStarts
+    [NG + 1] (int64) and the local ids of each row in ascending order (a
+    counting sort in oracle_omp.c)."""
+    ids = _i32(ids)
+    starts = np.zeros(int(NG) + 1, dtype=np.int64)
+    local = np.empty(int(np.count_nonzero(ids >= 0)), dtype=np.int32)
+    if _load_omp().oracle_rows(ids.size, int(NG), ids, starts, local) != 0:
+        raise MemoryError("oracle_rows: out of memory")
+    return starts, local
+
+
+def omp_gather(rows, qL, NG):
+    """BS6 on every core: one global row per iteration, ascending local order
+    from +0.0 (rows = rows_of(ids, NG))."""
+    starts, local = rows
+    qL = _f64(qL)
+    qG = np.empty(int(NG), dtype=np.float64)
+    _load_omp().oracle_omp_gather(qL.size, int(NG), starts, _i32(local), qL, qG)
+    return qG
