@@ -107,10 +107,10 @@ def _load_omp():
         lib = ctypes.CDLL(path)
         lib.oracle_omp_threads.restype = ctypes.c_int
         lib.oracle_omp_copy.argtypes = [_i64, _f64p, _f64p]
-        lib.oracle_omp_axpy.argtypes = [_i64, _dbl, _f64p, _dbl, _f64p]
+        lib.oracle_omp_axpy.argtypes = [_i64, _dbl, _f64p, _dbl, _f64p, _f64p]
         lib.oracle_omp_dot2.argtypes = [_i64, _f64p, _f64p]
         lib.oracle_omp_dot2.restype = _dbl
-        lib.oracle_omp_cg_update.argtypes = [_i64, _dbl, _f64p, _f64p, _f64p, _f64p]
+        lib.oracle_omp_cg_update.argtypes = [_i64, _dbl, _f64p, _f64p, _f64p, _f64p, _f64p, _f64p]
         lib.oracle_omp_scatter.argtypes = [_i64, _i32p, _f64p, _f64p]
         _i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
         lib.oracle_omp_gather.argtypes = [_i64, _i64, _i64p, _i32p, _f64p, _f64p]
@@ -306,10 +306,10 @@ def omp_copy(x):
 
 
 def omp_axpy(alpha, x, beta, y):
-    x = _f64(x)
-    out = np.array(y, dtype=np.float64, copy=True, order="C")
-    assert out.size == x.size
-    _load_omp().oracle_omp_axpy(x.size, float(alpha), x, float(beta), out)
+    x, y = _f64(x), _f64(y)
+    assert y.size == x.size
+    out = np.empty_like(x)
+    _load_omp().oracle_omp_axpy(x.size, float(alpha), x, float(beta), y, out)
     return out
 
 
@@ -325,13 +325,12 @@ def omp_norm(x):
 
 
 def omp_cg_update(alpha, p, Ap, x, r):
-    p, Ap = _f64(p), _f64(Ap)
-    xo = np.array(x, dtype=np.float64, copy=True, order="C")
-    ro = np.array(r, dtype=np.float64, copy=True, order="C")
+    p, Ap, x, r = _f64(p), _f64(Ap), _f64(x), _f64(r)
     n = p.size
-    assert Ap.size == n and xo.size == n and ro.size == n
+    assert Ap.size == n and x.size == n and r.size == n
+    xo, ro = np.empty_like(p), np.empty_like(p)
     lib = _load_omp()
-    lib.oracle_omp_cg_update(n, float(alpha), p, Ap, xo, ro)
+    lib.oracle_omp_cg_update(n, float(alpha), p, Ap, x, r, xo, ro)
     return xo, ro, float(lib.oracle_omp_dot2(n, ro, ro))
 
 

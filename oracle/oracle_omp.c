@@ -3,8 +3,9 @@
  * oracle.c (binary64, explicit fma, no contraction), split over threads:
  *
  *   copy, AXPY, BS5's vector updates, scatter: static chunks of the index
- *   range; every element is computed exactly as in oracle.c, so the results
- *   are bitwise the oracle's.
+ *   range, results written to fresh arrays inside the loop (no separate copy
+ *   of the inputs); every element is computed exactly as in oracle.c, so the
+ *   results are bitwise the oracle's.
  *
  *   gather: one global row per iteration (CSR rowStarts/localIds, local ids
  *   ascending within a row), summed from +0.0 in ascending local order --
@@ -32,12 +33,14 @@ void oracle_omp_copy(int64_t n, const double *x, double *y)
         y[i] = x[i];
 }
 
-void oracle_omp_axpy(int64_t n, double alpha, const double *x, double beta, double *y)
+/* out_i = fma(alpha, x_i, beta * y_i) (out may be y). */
+void oracle_omp_axpy(int64_t n, double alpha, const double *x, double beta, const double *y,
+                     double *out)
 {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         double by = beta * y[i];
-        y[i] = fma(alpha, x[i], by);
+        out[i] = fma(alpha, x[i], by);
     }
 }
 
@@ -89,14 +92,16 @@ double oracle_omp_dot2(int64_t n, const double *x, const double *y)
     return p + s;
 }
 
-void oracle_omp_cg_update(int64_t n, double alpha, const double *p, const double *Ap, double *x,
-                          double *r)
+/* xo_i = fma(alpha, p_i, x_i), ro_i = fma(-alpha, Ap_i, r_i) (xo may be x,
+ * ro may be r). */
+void oracle_omp_cg_update(int64_t n, double alpha, const double *p, const double *Ap,
+                          const double *x, const double *r, double *xo, double *ro)
 {
     double nalpha = -alpha;
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
-        x[i] = fma(alpha, p[i], x[i]);
-        r[i] = fma(nalpha, Ap[i], r[i]);
+        xo[i] = fma(alpha, p[i], x[i]);
+        ro[i] = fma(nalpha, Ap[i], r[i]);
     }
 }
 
