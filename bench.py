@@ -530,7 +530,7 @@ def all_cores_baseline(cfg, seconds, ids=None):
             cmd.append(path)
         try:
             res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True,
-                                 timeout=6 * seconds + 300)
+                                 timeout=3 * seconds + 180)
         except subprocess.TimeoutExpired:
             return {"unavailable": "the all-core oracle run did not finish in time"}
     lines = res.stdout.strip().splitlines()

@@ -82,3 +82,20 @@ def test_traffic_from_per_kernel_captures(tmp_path, monkeypatch):
     assert doc["norm"]["measured_bytes"] == 5e7 and doc["dot"]["measured_bytes"] == 9e7
     assert abs(doc["norm"]["scale"] - tw.NL / cw.NL) < 1e-12
     assert "scatter" not in doc and "copy" not in doc   # not captured
+
+
+def test_all_cores_leg_reports_a_figure_or_why_not():
+    """cpu_baseline.all_cores: the oracle's loops on every core, run in a
+    process of its own; a figure with its thread count and per-operation
+    split, or -- without an OpenMP compiler -- an `unavailable` reason."""
+    import bench
+    import oracle
+    cfg = bench.gen.WORKLOADS["tiny"]
+    rec = bench.all_cores_baseline(cfg, 0.2)
+    if oracle.build_omp() is None:
+        assert "unavailable" in rec
+        return
+    assert rec["unit"] == "GB/s" and rec["value"] > 0 and rec["cores"] >= 1
+    assert set(rec["per_op"]) == {"copy", "axpy", "norm", "dot", "cg_update", "gather", "scatter",
+                                  "cg_iteration"}
+    assert all(v["GB/s"] > 0 for v in rec["per_op"].values())
